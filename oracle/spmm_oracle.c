@@ -1,0 +1,91 @@
+/*
+ * CPU oracle for CSR SpMM -- TEST INFRASTRUCTURE, not part of the product.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load this file's library.  It shares no code, header or table with the
+ * CUDA library: it is a plain single-threaded C restatement of the
+ * operation's definition, accumulating in double precision.
+ *
+ * Definition followed (SpMM, page "Performance Optimization of Deep Learning
+ * Sparse Matrix Kernels on Intel Max Series GPU", SPMM section, Fig. 5 and
+ * Algorithm 2): row C_i of the dense output is produced by walking the
+ * nonzeros of sparse row A_i; for the nonzero with value s at column k the
+ * scaled dense row s * B_k is added to C_i (a SAXPY).  C_i starts at zero
+ * and is written once.  In index form
+ *
+ *     C[i][n] = sum_{p = rowptr[i]}^{rowptr[i+1]-1} vals[p] * B[colind[p]][n].
+ *
+ * The Sgap page ("Sgap: Towards Efficient Sparse Tensor Algebra Compilation
+ * for GPU", sparse-dense hybrid algebra section) states the same reduction:
+ * SpMM reduces over the sparse dimension j.  The kkmem page ("Sparse
+ * Matrix-Matrix Multiplication on Multilevel Memory Architectures", access
+ * pattern observations) describes the same row-by-row order: A streamed,
+ * each C row written once, B row j read once per nonzero in column j.
+ *
+ * Beside C the oracle returns S[i][n] = sum_p |vals[p] * B[colind[p]][n]|,
+ * the magnitude sum that scales the acceptance bound of a floating-point
+ * result (|C_gpu - C| <= rel * S + abs).
+ *
+ * Readings where the pages are silent: duplicate (i, j) entries are summed;
+ * column order inside a row is free; an empty row gives an exact zero row;
+ * C is overwritten, never accumulated into.  bf16 B values are decoded from
+ * their bit patterns as the upper half of an IEEE-754 binary32 (exact).
+ *
+ * Every floating-point step is a double-precision multiply and add, with
+ * contraction disabled at build time (-ffp-contract=off), so results are the
+ * same on every host.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* bfloat16 is the top 16 bits of a binary32; decoding is a bit move. */
+static double oracle_bf16_to_double(uint16_t bits) {
+  uint32_t w = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+static double oracle_b_value(const void* B, int32_t b_is_bf16, int64_t idx) {
+  if (b_is_bf16) return oracle_bf16_to_double(((const uint16_t*)B)[idx]);
+  return (double)((const float*)B)[idx];
+}
+
+/*
+ * C_out[t][n], S_out[t][n] for the rows listed in rows[0..nrows) (all rows
+ * 0..M-1 in order when rows == NULL, nrows then ignored).  B has K rows of N
+ * values.  S_out may be NULL.  Returns 0; -1 on an argument error (bad
+ * sizes, a listed row outside [0, M)); -2 when a visited row's rowptr range
+ * is decreasing or a visited column index lies outside [0, K).
+ */
+int spmm_oracle_rows_f64(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
+                         const int32_t* colind, const float* vals, const void* B,
+                         int32_t b_is_bf16, const int32_t* rows, int64_t nrows, double* C_out,
+                         double* S_out) {
+  if (M < 0 || K < 0 || N < 0 || !rowptr || !C_out) return -1;
+  if (rows == NULL) nrows = M;
+  for (int64_t t = 0; t < nrows; ++t) {
+    int32_t i = rows ? rows[t] : (int32_t)t;
+    if (i < 0 || i >= M) return -1;
+    double* c = C_out + t * (int64_t)N;
+    double* s = S_out ? S_out + t * (int64_t)N : NULL;
+    for (int32_t n = 0; n < N; ++n) {
+      c[n] = 0.0;
+      if (s) s[n] = 0.0;
+    }
+    if (rowptr[i + 1] < rowptr[i]) return -2;
+    for (int64_t p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+      double a = (double)vals[p];
+      int64_t row_of_b = colind[p];
+      if (row_of_b < 0 || row_of_b >= K) return -2;
+      for (int32_t n = 0; n < N; ++n) {
+        double prod = a * oracle_b_value(B, b_is_bf16, row_of_b * N + n);
+        c[n] += prod;
+        if (s) s[n] += fabs(prod);
+      }
+    }
+  }
+  return 0;
+}
