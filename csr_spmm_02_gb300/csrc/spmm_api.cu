@@ -1,0 +1,153 @@
+// C ABI entry points: exec with a plan, the one-call forms, status strings.
+#include <cstdint>
+
+#include "spmm_internal.h"
+
+spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N, int32_t kernel,
+                           int32_t items_per_cta, cudaStream_t stream, bool stream_ordered,
+                           spmm_plan_t* plan_out);
+void spmm_free_plan(spmm_plan_t plan, cudaStream_t stream);
+
+namespace spmm {
+
+static int pow2_at_least(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+Shape choose_shape(int32_t N, bool bf16, bool vector_ok) {
+  const int vec = bf16 ? 8 : 4;
+  if (vector_ok) {
+    const int lanes = N / vec;  // N is a multiple of vec here
+    if (lanes <= 32) return Shape{vec, pow2_at_least(lanes), 1};
+    if (lanes <= 64) return Shape{vec, 32, 2};
+    return Shape{vec, 32, bf16 ? 2 : 4};  // wider N runs as several column tiles
+  }
+  return N <= 8 ? Shape{1, 8, 1} : Shape{1, 32, 1};
+}
+
+}  // namespace spmm
+
+using namespace spmm;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+struct DeviceGuard {  // run on the plan's device, restore the caller's afterwards
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* vals, const void* B,
+                 bool bf16, float* C, cudaStream_t stream) {
+  if (!plan) return SPMM_ERR_PLAN_MISMATCH;
+  if (K < 0) return SPMM_ERR_INVALID_ARG;
+  if (plan->M == 0 || plan->N == 0) return SPMM_OK;
+  if (!C || (plan->nnz > 0 && (!colind || !vals || !B || K == 0))) return SPMM_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return SPMM_ERR_CUDA;
+
+  const bool vector_ok = plan->N % (bf16 ? 8 : 4) == 0 && aligned16(B) && aligned16(C);
+  const Shape s = choose_shape(plan->N, bf16, vector_ok);
+  Launch L{};
+  L.M = plan->M;
+  L.N = plan->N;
+  L.nnz = plan->nnz;
+  L.rowptr = plan->rowptr;
+  L.colind = colind;
+  L.vals = vals;
+  L.B = B;
+  L.C = C;
+  L.part = plan->part;
+  L.num_ctas = plan->num_ctas;
+  L.items_per_cta = plan->items_per_cta;
+  L.carry = plan->carry;
+  L.err = plan->err;
+  L.stream = stream;
+
+  cudaError_t e;
+  if (plan->kernel == SPMM_KERNEL_ROW) {
+    e = bf16 ? launch_row_bf16(L, s) : launch_row_f32(L, s);
+    if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+  } else {
+    e = bf16 ? launch_balanced_bf16(L, s) : launch_balanced_f32(L, s);
+    if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+    if (e == cudaSuccess) e = launch_fixup(L);
+  }
+  return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+}
+
+spmm_status one_call(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, const int32_t* colind,
+                     const float* vals, const void* B, bool bf16, float* C, void* stream) {
+  if (M < 0 || K < 0 || N < 0) return SPMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return SPMM_OK;
+  if (!rowptr) return SPMM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // nnz = rowptr[M] is needed on the host to size the plan.
+  int32_t nnz = 0;
+  if (cudaMemcpyAsync(&nnz, rowptr + M, sizeof nnz, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return SPMM_ERR_CUDA;
+  if (nnz < 0) return SPMM_ERR_INVALID_CSR;
+  spmm_plan_t plan = nullptr;
+  spmm_status st = spmm_make_plan(rowptr, M, nnz, N, SPMM_KERNEL_AUTO, 0, s, true, &plan);
+  if (st != SPMM_OK) return st;
+  st = exec(plan, K, colind, vals, B, bf16, C, s);
+  spmm_free_plan(plan, s);
+  return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+spmm_status spmm_csr_f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* vals,
+                              const float* B, float* C, void* stream) {
+  return exec(plan, K, colind, vals, B, false, C, static_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_csr_bf16f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* vals,
+                                  const uint16_t* B, float* C, void* stream) {
+  return exec(plan, K, colind, vals, B, true, C, static_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_csr_f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, const int32_t* colind,
+                         const float* vals, const float* B, float* C, void* stream) {
+  return one_call(M, K, N, rowptr, colind, vals, B, false, C, stream);
+}
+
+spmm_status spmm_csr_bf16f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, const int32_t* colind,
+                             const float* vals, const uint16_t* B, float* C, void* stream) {
+  return one_call(M, K, N, rowptr, colind, vals, B, true, C, stream);
+}
+
+spmm_status spmm_plan_set_split_event(spmm_plan_t plan, void* event) {
+  if (!plan) return SPMM_ERR_INVALID_ARG;
+  plan->split_event = static_cast<cudaEvent_t>(event);
+  return SPMM_OK;
+}
+
+const char* spmm_status_string(spmm_status status) {
+  switch (status) {
+    case SPMM_OK: return "SPMM_OK";
+    case SPMM_ERR_INVALID_ARG: return "SPMM_ERR_INVALID_ARG";
+    case SPMM_ERR_INVALID_CSR: return "SPMM_ERR_INVALID_CSR";
+    case SPMM_ERR_UNSUPPORTED: return "SPMM_ERR_UNSUPPORTED";
+    case SPMM_ERR_PLAN_MISMATCH: return "SPMM_ERR_PLAN_MISMATCH";
+    case SPMM_ERR_CUDA: return "SPMM_ERR_CUDA";
+    case SPMM_ERR_DEVICE_TIMEOUT: return "SPMM_ERR_DEVICE_TIMEOUT";
+  }
+  return "SPMM_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Host-side internals shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/spmm.h"
+
+struct spmm_plan_s {
+  int32_t M = 0;
+  int64_t nnz = 0;
+  int32_t N = 0;
+  const int32_t* rowptr = nullptr;  // device, borrowed from the caller
+  int32_t kernel = SPMM_KERNEL_ROW;
+  int32_t max_row_nnz = 0;
+  int32_t empty_rows = 0;
+  int32_t items_per_cta = 0;  // balanced only
+  int32_t num_ctas = 0;       // balanced only
+  int device = 0;
+  bool stream_ordered = false;  // workspace from cudaMallocAsync (one-call form)
+  // device workspace (one allocation, carved up)
+  void* workspace = nullptr;
+  int64_t workspace_bytes = 0;
+  int2* part = nullptr;   // [num_ctas + 1] merge-path coordinates (row, nnz)
+  float* carry = nullptr; // [num_ctas][2][N] partial rows split across CTAs
+  int* err = nullptr;     // device error word
+  int* stats = nullptr;   // [2]: max row length, empty rows
+  cudaEvent_t split_event = nullptr;  // recorded between main kernel and fixup
+};
+
+namespace spmm {
+
+// Everything one SpMM launch needs (device pointers).
+struct Launch {
+  int32_t M, N;
+  int64_t nnz;
+  const int32_t* rowptr;
+  const int32_t* colind;
+  const float* vals;
+  const void* B;
+  float* C;
+  // balanced kernel
+  const int2* part;
+  int32_t num_ctas;
+  int32_t items_per_cta;
+  float* carry;
+  int* err;
+  cudaStream_t stream;
+};
+
+// Lane layout for one launch: VEC elements per 16-byte load, G lanes per row
+// group (a power of two <= 32), NCH vector chunks per lane.  A group covers
+// TW = G * VEC * NCH output columns; wider N is split into column tiles.
+struct Shape {
+  int vec, G, nch;
+  int tile_width() const { return G * vec * nch; }
+};
+
+Shape choose_shape(int32_t N, bool bf16, bool vector_ok);
+
+cudaError_t launch_row_f32(const Launch& L, Shape s);
+cudaError_t launch_row_bf16(const Launch& L, Shape s);
+cudaError_t launch_balanced_f32(const Launch& L, Shape s);
+cudaError_t launch_balanced_bf16(const Launch& L, Shape s);
+cudaError_t launch_fixup(const Launch& L);
+
+
+constexpr int kDefaultItemsPerCta = 2048;
+constexpr int kMaxItemsPerCta = 8192;
+constexpr int kMaxDevices = 64;
+
+}  // namespace spmm

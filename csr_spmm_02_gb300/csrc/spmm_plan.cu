@@ -1,0 +1,282 @@
+// Plan construction (row statistics, kernel choice, merge-path partition),
+// CSR validation and the deterministic fixup of rows split across CTAs.
+#include <algorithm>
+#include <cstdint>
+#include <new>
+
+#include "spmm_device.cuh"
+#include "spmm_internal.h"
+
+namespace spmm {
+
+// stats[0] = longest row, stats[1] = number of empty rows.
+__global__ void __launch_bounds__(kThreads) row_stats_kernel(const int32_t* __restrict__ rowptr, int32_t M,
+                                                             int* __restrict__ stats) {
+  int longest = 0, empty = 0;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < M; i += int64_t(gridDim.x) * blockDim.x) {
+    const int len = __ldg(rowptr + i + 1) - __ldg(rowptr + i);
+    longest = max(longest, len);
+    empty += len == 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
+    empty += __shfl_xor_sync(0xffffffffu, empty, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicMax(stats, longest);
+    atomicAdd(stats + 1, empty);
+  }
+}
+
+// part[c] = (row, nonzero) where the merged sequence of nonzeros and row ends
+// is cut at diagonal d = min(c * T, M + nnz): the row is the number of rows
+// whose end position rowptr[r+1] + r lies before d.
+__global__ void __launch_bounds__(kThreads) merge_path_partition_kernel(const int32_t* __restrict__ rowptr,
+                                                                        int32_t M, int64_t nnz, int64_t T,
+                                                                        int32_t P, int2* __restrict__ part) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c > P) return;
+  const int64_t d = min(int64_t(c) * T, int64_t(M) + nnz);
+  int lo = 0, hi = M;
+  while (lo < hi) {
+    const int mid = lo + ((hi - lo) >> 1);
+    if (int64_t(__ldg(rowptr + mid + 1)) + mid >= d) hi = mid; else lo = mid + 1;
+  }
+  part[c] = make_int2(lo, int(d - lo));
+}
+
+// flag |= 1: rowptr[0] != 0, rowptr[M] != nnz or a decreasing step; |= 2: colind out of range.
+__global__ void __launch_bounds__(kThreads) validate_kernel(const int32_t* __restrict__ rowptr,
+                                                            const int32_t* __restrict__ colind, int32_t M,
+                                                            int32_t K, int64_t nnz, int* __restrict__ flag) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  int bad = 0;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i <= M; i += stride) {
+    const int v = rowptr[i];
+    if (i == 0 && v != 0) bad |= 1;
+    if (i == M && int64_t(v) != nnz) bad |= 1;
+    if (i < M && rowptr[i + 1] < v) bad |= 1;
+  }
+  for (int64_t p = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; p < nnz; p += stride) {
+    const int c = colind[p];
+    if (c < 0 || c >= K) bad |= 2;
+  }
+  if (bad) atomicOr(flag, bad);
+}
+
+// One warp per CTA range c.  If a row starts inside range c and runs past it
+// (its carry slot 1), add slot 1 of c and slot 0 of every following range up
+// to the one holding the row's end, in range order, and write the C row.
+__global__ void __launch_bounds__(kThreads) spmm_fixup_kernel(int32_t M, int32_t N,
+                                                              const int32_t* __restrict__ rowptr,
+                                                              const int2* __restrict__ part, int32_t P,
+                                                              const float* __restrict__ carry,
+                                                              float* __restrict__ C) {
+  const int c = blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (c >= P) return;
+  const int2 beg = __ldg(part + c);
+  const int2 fin = __ldg(part + c + 1);
+  const int row = fin.x;
+  if (row >= M) return;
+  const int rs = __ldg(rowptr + row);
+  if (rs < beg.y || rs >= fin.y) return;  // no row starts in range c and continues past it
+  int last = c + 1;
+  while (__ldg(part + last + 1).x == row) ++last;  // range `last` holds the row's end
+  for (int n = lane; n < N; n += 32) {
+    float s = carry[(size_t(c) * 2 + 1) * N + n];
+    for (int c2 = c + 1; c2 <= last; ++c2) s += carry[(size_t(c2) * 2) * N + n];
+    __stcs(C + size_t(row) * N + n, s);
+  }
+}
+
+cudaError_t launch_fixup(const Launch& L) {
+  constexpr int kWarps = kThreads / 32;
+  const unsigned grid = unsigned((L.num_ctas + kWarps - 1) / kWarps);
+  spmm_fixup_kernel<<<grid, kThreads, 0, L.stream>>>(L.M, L.N, L.rowptr, L.part, L.num_ctas, L.carry, L.C);
+  return cudaGetLastError();
+}
+
+}  // namespace spmm
+
+using namespace spmm;
+
+namespace {
+
+cudaError_t dev_alloc(void** p, size_t bytes, bool stream_ordered, cudaStream_t s) {
+  return stream_ordered ? cudaMallocAsync(p, bytes, s) : cudaMalloc(p, bytes);
+}
+void dev_free(void* p, bool stream_ordered, cudaStream_t s) {
+  if (!p) return;
+  if (stream_ordered) cudaFreeAsync(p, s); else cudaFree(p);
+}
+
+unsigned stats_grid(int32_t M) {
+  const int64_t blocks = (int64_t(M) + kThreads - 1) / kThreads;
+  return unsigned(std::max<int64_t>(1, std::min<int64_t>(blocks, 152 * 8)));
+}
+
+}  // namespace
+
+// Plan construction shared by spmm_csr_plan(_ex) and the one-call forms.
+spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N, int32_t kernel,
+                           int32_t items_per_cta, cudaStream_t stream, bool stream_ordered,
+                           spmm_plan_t* plan_out) {
+  if (!plan_out) return SPMM_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  if (M < 0 || N < 0 || nnz < 0) return SPMM_ERR_INVALID_ARG;
+  if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+  if (M > 0 && !rowptr) return SPMM_ERR_INVALID_ARG;
+  if (kernel < SPMM_KERNEL_AUTO || kernel > SPMM_KERNEL_BALANCED) return SPMM_ERR_INVALID_ARG;
+  if (items_per_cta != 0 && (items_per_cta < 256 || items_per_cta > kMaxItemsPerCta || items_per_cta % 256 != 0))
+    return SPMM_ERR_INVALID_ARG;
+
+  spmm_plan_s* plan = new (std::nothrow) spmm_plan_s();
+  if (!plan) return SPMM_ERR_CUDA;
+  plan->M = M;
+  plan->nnz = nnz;
+  plan->N = N;
+  plan->rowptr = rowptr;
+  plan->stream_ordered = stream_ordered;
+  plan->kernel = kernel == SPMM_KERNEL_BALANCED ? SPMM_KERNEL_BALANCED : SPMM_KERNEL_ROW;
+  if (cudaGetDevice(&plan->device) != cudaSuccess) {
+    delete plan;
+    return SPMM_ERR_CUDA;
+  }
+  if (M == 0 || N == 0) {  // nothing to compute; exec is a no-op
+    *plan_out = plan;
+    return SPMM_OK;
+  }
+
+  auto fail = [&](cudaError_t) {
+    dev_free(plan->workspace, stream_ordered, stream);
+    dev_free(plan->err, stream_ordered, stream);
+    delete plan;
+    return SPMM_ERR_CUDA;
+  };
+
+  // error word + statistics (16 bytes)
+  void* small = nullptr;
+  cudaError_t e = dev_alloc(&small, 16, stream_ordered, stream);
+  if (e != cudaSuccess) return fail(e);
+  plan->err = static_cast<int*>(small);
+  plan->stats = plan->err + 1;
+  if ((e = cudaMemsetAsync(small, 0, 16, stream)) != cudaSuccess) return fail(e);
+  row_stats_kernel<<<stats_grid(M), kThreads, 0, stream>>>(rowptr, M, plan->stats);
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
+  int host_stats[2] = {0, 0};
+  if ((e = cudaMemcpyAsync(host_stats, plan->stats, sizeof host_stats, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return fail(e);
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return fail(e);
+  plan->max_row_nnz = host_stats[0];
+  plan->empty_rows = host_stats[1];
+
+  if (kernel == SPMM_KERNEL_AUTO) {
+    // Short, even rows: one group per row keeps all lanes busy with no
+    // partition or fixup.  Skewed rows (a row far longer than the mean): the
+    // merge-path split bounds every CTA's work.
+    const double mean = double(nnz) / double(M);
+    plan->kernel = double(plan->max_row_nnz) <= 4.0 * mean + 32.0 ? SPMM_KERNEL_ROW : SPMM_KERNEL_BALANCED;
+  }
+
+  if (plan->kernel == SPMM_KERNEL_BALANCED) {
+    const int T = items_per_cta ? items_per_cta : kDefaultItemsPerCta;
+    const int64_t total = int64_t(M) + nnz;
+    const int64_t P = (total + T - 1) / T;
+    if (P > INT32_MAX - 1) return fail(cudaErrorInvalidValue);
+    plan->items_per_cta = T;
+    plan->num_ctas = int32_t(P);
+    const size_t part_bytes = (size_t(P) + 1) * sizeof(int2);
+    const size_t part_padded = (part_bytes + 255) & ~size_t(255);
+    const size_t carry_bytes = size_t(P) * 2 * size_t(N) * sizeof(float);
+    plan->workspace_bytes = int64_t(part_padded + carry_bytes);
+    if ((e = dev_alloc(&plan->workspace, part_padded + carry_bytes, stream_ordered, stream)) != cudaSuccess)
+      return fail(e);
+    plan->part = static_cast<int2*>(plan->workspace);
+    plan->carry = reinterpret_cast<float*>(static_cast<char*>(plan->workspace) + part_padded);
+    const unsigned grid = unsigned((P + 1 + kThreads - 1) / kThreads);
+    merge_path_partition_kernel<<<grid, kThreads, 0, stream>>>(rowptr, M, nnz, T, int32_t(P), plan->part);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
+  }
+  plan->workspace_bytes += 16;
+  *plan_out = plan;
+  return SPMM_OK;
+}
+
+void spmm_free_plan(spmm_plan_t plan, cudaStream_t stream) {
+  if (!plan) return;
+  dev_free(plan->workspace, plan->stream_ordered, stream);
+  dev_free(plan->err, plan->stream_ordered, stream);
+  delete plan;
+}
+
+extern "C" {
+
+spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N, int32_t kernel,
+                             int32_t items_per_cta, void* stream, spmm_plan_t* plan_out) {
+  return spmm_make_plan(rowptr, M, nnz, N, kernel, items_per_cta, static_cast<cudaStream_t>(stream), false,
+                        plan_out);
+}
+
+spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N, void* stream,
+                          spmm_plan_t* plan_out) {
+  return spmm_csr_plan_ex(rowptr, M, nnz, N, SPMM_KERNEL_AUTO, 0, stream, plan_out);
+}
+
+spmm_status spmm_plan_get_info(spmm_plan_t plan, spmm_plan_info* info) {
+  if (!plan || !info) return SPMM_ERR_INVALID_ARG;
+  info->kernel = plan->kernel;
+  info->M = plan->M;
+  info->nnz = plan->nnz;
+  info->N = plan->N;
+  info->max_row_nnz = plan->max_row_nnz;
+  info->empty_rows = plan->empty_rows;
+  info->items_per_cta = plan->items_per_cta;
+  info->num_ctas = plan->num_ctas;
+  info->workspace_bytes = plan->workspace_bytes;
+  return SPMM_OK;
+}
+
+spmm_status spmm_plan_destroy(spmm_plan_t plan) {
+  if (!plan) return SPMM_OK;
+  if (plan->stream_ordered) cudaDeviceSynchronize();
+  spmm_free_plan(plan, nullptr);
+  return SPMM_OK;
+}
+
+spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream) {
+  if (!plan) return SPMM_ERR_INVALID_ARG;
+  if (!plan->err) return SPMM_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, plan->err, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SPMM_ERR_CUDA;
+  if (cudaMemsetAsync(plan->err, 0, sizeof word, s) != cudaSuccess) return SPMM_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SPMM_ERR_CUDA;
+  return word ? SPMM_ERR_DEVICE_TIMEOUT : SPMM_OK;
+}
+
+spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int32_t M, int32_t K, int64_t nnz,
+                              void* stream) {
+  if (M < 0 || K < 0 || nnz < 0) return SPMM_ERR_INVALID_ARG;
+  if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+  if (!rowptr || (nnz > 0 && !colind)) return SPMM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* flag = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&flag), sizeof(int), s) != cudaSuccess) return SPMM_ERR_CUDA;
+  int host = 0;
+  cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(int), s);
+  if (e == cudaSuccess) {
+    const int64_t work = std::max<int64_t>(int64_t(M) + 1, nnz);
+    const unsigned grid = unsigned(std::max<int64_t>(1, std::min<int64_t>((work + kThreads - 1) / kThreads, 152 * 16)));
+    validate_kernel<<<grid, kThreads, 0, s>>>(rowptr, colind, M, K, nnz, flag);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&host, flag, sizeof(int), cudaMemcpyDeviceToHost, s);
+  cudaFreeAsync(flag, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return SPMM_ERR_CUDA;
+  return host ? SPMM_ERR_INVALID_CSR : SPMM_OK;
+}
+
+}  // extern "C"

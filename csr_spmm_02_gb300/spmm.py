@@ -1,0 +1,212 @@
+"""Thin ctypes binding over the C ABI in ``include/spmm.h``.
+
+Argument marshalling only: every step of the multiplication runs in the CUDA
+library ``_lib/libcsr_spmm_gb300.so``.  There is no CPU fallback; if the
+library is missing, importing the functions below raises.
+
+Functions carry the C names:
+
+* ``spmm_csr_plan(rowptr, M, nnz, N, kernel=..., items_per_cta=0)`` -> Plan
+* ``spmm_csr_f32_exec(plan, K, colind, vals, B, C)``
+* ``spmm_csr_bf16f32_exec(plan, K, colind, vals, B_bits, C)``
+* ``spmm_csr_f32(M, K, N, rowptr, colind, vals, B, C)``
+* ``spmm_csr_bf16f32(M, K, N, rowptr, colind, vals, B_bits, C)``
+* ``spmm_csr_validate(rowptr, colind, M, K, nnz)``
+* ``spmm_plan_check_device(plan)``
+
+Tensors are CUDA tensors: rowptr/colind int32, vals float32, B float32 (or a
+uint16/int16/bfloat16 tensor holding bf16 bits), C float32, all contiguous.
+Calls run on the current torch CUDA stream unless ``stream`` is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+SPMM_OK = 0
+STATUS_NAMES = {0: "SPMM_OK", 1: "SPMM_ERR_INVALID_ARG", 2: "SPMM_ERR_INVALID_CSR",
+                3: "SPMM_ERR_UNSUPPORTED", 4: "SPMM_ERR_PLAN_MISMATCH", 5: "SPMM_ERR_CUDA",
+                6: "SPMM_ERR_DEVICE_TIMEOUT"}
+KERNELS = {"auto": 0, "row": 1, "balanced": 2}
+KERNEL_NAMES = {1: "row", 2: "balanced"}
+
+EXPORTS = ["spmm_csr_plan", "spmm_csr_plan_ex", "spmm_plan_get_info", "spmm_plan_destroy",
+           "spmm_csr_f32_exec", "spmm_csr_bf16f32_exec", "spmm_csr_f32", "spmm_csr_bf16f32",
+           "spmm_csr_validate", "spmm_plan_check_device", "spmm_plan_set_split_event",
+           "spmm_status_string"]
+
+
+class SpmmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("M", ctypes.c_int32), ("nnz", ctypes.c_int64),
+                ("N", ctypes.c_int32), ("max_row_nnz", ctypes.c_int32), ("empty_rows", ctypes.c_int32),
+                ("items_per_cta", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Open the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA SpMM library not built ({p}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    sig = {
+        "spmm_csr_plan": [vp, i32, i64, i32, vp, ctypes.POINTER(vp)],
+        "spmm_csr_plan_ex": [vp, i32, i64, i32, i32, i32, vp, ctypes.POINTER(vp)],
+        "spmm_plan_get_info": [vp, ctypes.POINTER(PlanInfo)],
+        "spmm_plan_destroy": [vp],
+        "spmm_csr_f32_exec": [vp, i32, vp, vp, vp, vp, vp],
+        "spmm_csr_bf16f32_exec": [vp, i32, vp, vp, vp, vp, vp],
+        "spmm_csr_f32": [i32, i32, i32, vp, vp, vp, vp, vp, vp],
+        "spmm_csr_bf16f32": [i32, i32, i32, vp, vp, vp, vp, vp, vp],
+        "spmm_csr_validate": [vp, vp, i32, i32, i64, vp],
+        "spmm_plan_check_device": [vp, vp],
+        "spmm_plan_set_split_event": [vp, vp],
+        "spmm_status_string": [ctypes.c_int],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_char_p if name == "spmm_status_string" else ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != SPMM_OK:
+        raise SpmmError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t, dtype, name, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+_I32 = (torch.int32,)
+_F32 = (torch.float32,)
+_BF16_BITS = (torch.uint16, torch.int16, torch.bfloat16) if hasattr(torch, "uint16") else (torch.int16, torch.bfloat16)
+
+
+class Plan:
+    """Owns a ``spmm_plan_t``; keeps the rowptr tensor alive while the plan lives."""
+
+    def __init__(self, handle: int, rowptr: torch.Tensor):
+        self.handle = ctypes.c_void_p(handle)
+        self.rowptr = rowptr
+
+    def info(self) -> dict:
+        pi = PlanInfo()
+        _check(load().spmm_plan_get_info(self.handle, ctypes.byref(pi)), "spmm_plan_get_info")
+        d = {name: getattr(pi, name) for name, _ in PlanInfo._fields_}
+        d["kernel"] = KERNEL_NAMES.get(d["kernel"], d["kernel"])
+        return d
+
+    def destroy(self):
+        if self.handle:
+            load().spmm_plan_destroy(self.handle)
+            self.handle = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def spmm_csr_plan(rowptr, M, nnz, N, kernel="auto", items_per_cta=0, stream=None) -> Plan:
+    out = ctypes.c_void_p()
+    st = load().spmm_csr_plan_ex(_ptr(rowptr, _I32, "rowptr"), M, nnz, N, KERNELS[kernel], items_per_cta,
+                                 _stream(stream), ctypes.byref(out))
+    _check(st, "spmm_csr_plan")
+    return Plan(out.value, rowptr)
+
+
+def spmm_csr_f32_exec(plan: Plan, K, colind, vals, B, C, stream=None):
+    _check(load().spmm_csr_f32_exec(plan.handle, K, _ptr(colind, _I32, "colind", True),
+                                    _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True),
+                                    _ptr(C, _F32, "C"), _stream(stream)), "spmm_csr_f32_exec")
+    return C
+
+
+def spmm_csr_bf16f32_exec(plan: Plan, K, colind, vals, B, C, stream=None):
+    _check(load().spmm_csr_bf16f32_exec(plan.handle, K, _ptr(colind, _I32, "colind", True),
+                                        _ptr(vals, _F32, "vals", True), _ptr(B, _BF16_BITS, "B", True),
+                                        _ptr(C, _F32, "C"), _stream(stream)), "spmm_csr_bf16f32_exec")
+    return C
+
+
+def spmm_csr_f32(M, K, N, rowptr, colind, vals, B, C, stream=None):
+    _check(load().spmm_csr_f32(M, K, N, _ptr(rowptr, _I32, "rowptr"), _ptr(colind, _I32, "colind", True),
+                               _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True), _ptr(C, _F32, "C"),
+                               _stream(stream)), "spmm_csr_f32")
+    return C
+
+
+def spmm_csr_bf16f32(M, K, N, rowptr, colind, vals, B, C, stream=None):
+    _check(load().spmm_csr_bf16f32(M, K, N, _ptr(rowptr, _I32, "rowptr"), _ptr(colind, _I32, "colind", True),
+                                   _ptr(vals, _F32, "vals", True), _ptr(B, _BF16_BITS, "B", True),
+                                   _ptr(C, _F32, "C"), _stream(stream)), "spmm_csr_bf16f32")
+    return C
+
+
+def spmm_csr_validate(rowptr, colind, M, K, nnz, stream=None) -> int:
+    """Return the status code (SPMM_OK or SPMM_ERR_INVALID_CSR); raise on other errors."""
+    st = load().spmm_csr_validate(_ptr(rowptr, _I32, "rowptr"), _ptr(colind, _I32, "colind", True), M, K, nnz,
+                                  _stream(stream))
+    if st not in (0, 2):
+        raise SpmmError(st, "spmm_csr_validate")
+    return st
+
+
+def spmm_plan_check_device(plan: Plan, stream=None) -> int:
+    return load().spmm_plan_check_device(plan.handle, _stream(stream))
+
+
+def spmm_plan_set_split_event(plan: Plan, event) -> None:
+    """Record `event` (a torch.cuda.Event, or None) after the main kernel of every exec."""
+    handle = None
+    if event is not None:
+        event.record()  # make sure the event exists before handing its handle over
+        handle = ctypes.c_void_p(event.cuda_event)
+    plan._split_event = event  # keep it alive while it is set
+    _check(load().spmm_plan_set_split_event(plan.handle, handle), "spmm_plan_set_split_event")
+
+
+def spmm_status_string(status: int) -> str:
+    return load().spmm_status_string(status).decode()

@@ -1,0 +1,185 @@
+/*
+ * csr_spmm_02_gb300 -- C ABI of the GB300 (sm_103a) CSR SpMM library.
+ *
+ * Operation (SpMM, page "Performance Optimization of Deep Learning Sparse
+ * Matrix Kernels on Intel Max Series GPU", SPMM section, Fig. 5 and
+ * Algorithm 2; the same reduction over the sparse index j is the core
+ * operation named on the page "Sgap: Towards Efficient Sparse Tensor Algebra
+ * Compilation for GPU", sparse-dense hybrid algebra section):
+ *
+ *     C[i][n] = sum_{p = rowptr[i]}^{rowptr[i+1]-1} vals[p] * B[colind[p]][n]
+ *
+ * for 0 <= i < M, 0 <= n < N.  A is M x K in CSR form; B (K x N) and C
+ * (M x N) are dense and row-major.  C is overwritten (never accumulated
+ * into); an empty row of A gives a zero row of C.  Duplicate (i, j) entries
+ * are summed and column indices need not be sorted.
+ *
+ * Types and layout
+ *   rowptr  int32[M+1], rowptr[0] = 0, non-decreasing, rowptr[M] = nnz
+ *   colind  int32[nnz], each in [0, K)
+ *   vals    fp32[nnz]
+ *   B       fp32[K*N], or bf16[K*N] passed as its raw uint16 bit patterns
+ *   C       fp32[M*N]
+ *   The bf16 variants widen B exactly to fp32 and accumulate in fp32.
+ *
+ * Pointers and ownership
+ *   Every array pointer is a DEVICE pointer owned by the caller; the library
+ *   never frees or retains them, except that a plan remembers `rowptr` and
+ *   reads it again on every exec (keep it alive and unchanged while the plan
+ *   is used).  The library writes only C and its own plan workspace.
+ *   `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  All calls are asynchronous on `stream` unless stated.
+ *
+ * Sizes
+ *   M, K, N >= 0; 0 <= nnz <= 2^31 - 1.  M = 0 or N = 0 is a successful no-op.
+ *   Any N >= 1 is supported.  16-byte vector paths are used when N is a
+ *   multiple of 4 (fp32 B) or 8 (bf16 B) and B and C are 16-byte aligned;
+ *   otherwise a scalar path runs with the same results.
+ *
+ * Results and determinism
+ *   No floating-point atomics are used: for a given plan, repeated calls give
+ *   bitwise-identical C.  The summation order differs from a sequential loop
+ *   (rows may be split into pieces that are combined in a fixed order).
+ *
+ * Errors
+ *   Every call returns a spmm_status; no exception crosses the ABI and no
+ *   kernel traps.  Argument errors are detected before any CUDA call.
+ *   Column indices outside [0, K) and malformed rowptr are NOT checked on
+ *   the fast path (undefined results); run spmm_csr_validate to check them.
+ *   A CUDA launch or API failure returns SPMM_ERR_CUDA.  Kernels that wait
+ *   on hardware copies give up after a bounded time and record
+ *   SPMM_ERR_DEVICE_TIMEOUT in the plan, read by spmm_plan_check_device.
+ */
+#ifndef CSR_SPMM_02_GB300_SPMM_H_
+#define CSR_SPMM_02_GB300_SPMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPMM_OK = 0,
+  SPMM_ERR_INVALID_ARG = 1,    /* bad size, NULL pointer, unknown option */
+  SPMM_ERR_INVALID_CSR = 2,    /* spmm_csr_validate found a malformed CSR */
+  SPMM_ERR_UNSUPPORTED = 3,    /* a size the library cannot handle (e.g. nnz >= 2^31) */
+  SPMM_ERR_PLAN_MISMATCH = 4,  /* exec called with a plan made for another shape */
+  SPMM_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
+  SPMM_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait expired (see above) */
+} spmm_status;
+
+/* Kernel family a plan uses. */
+typedef enum {
+  SPMM_KERNEL_AUTO = 0,      /* chosen from the row-length statistics */
+  SPMM_KERNEL_ROW = 1,       /* one (sub-)warp group per row: short, uniform rows */
+  SPMM_KERNEL_BALANCED = 2   /* merge-path nnz-balanced split + fixup: skewed rows */
+} spmm_kernel;
+
+/* Opaque plan: owns its device workspace (merge-path partition, carry rows
+ * of split rows, an error word).  Bound to (rowptr, M, nnz, N). */
+typedef struct spmm_plan_s* spmm_plan_t;
+
+/* What a plan decided (host copy, filled by spmm_plan_get_info). */
+typedef struct {
+  int32_t kernel;          /* SPMM_KERNEL_ROW or SPMM_KERNEL_BALANCED */
+  int32_t M;
+  int64_t nnz;
+  int32_t N;
+  int32_t max_row_nnz;     /* longest row of A */
+  int32_t empty_rows;      /* rows of A with no nonzero */
+  int32_t items_per_cta;   /* balanced: merge-path items (row ends + nonzeros) per CTA */
+  int32_t num_ctas;        /* balanced: number of merge-path ranges (CTAs) */
+  int64_t workspace_bytes; /* device bytes the plan owns */
+} spmm_plan_info;
+
+/*
+ * Build a plan for A's row structure (nnz-balanced row partitioning).
+ * Reads rowptr (device, M+1 entries) on `stream`: one small kernel computes
+ * the row-length statistics, which are copied to the host (this call
+ * synchronises `stream` once); for the balanced kernel a second kernel
+ * computes the merge-path partition (a binary search per range over the
+ * merged sequence of row ends and nonzeros -- the even nnz split the Sgap
+ * page's related work attributes to Yang et al., and the element-balanced
+ * EB scheme of its DA-SpMM design space).  The plan's workspace is
+ * allocated with cudaMalloc.  *plan_out receives the plan (NULL on error).
+ */
+spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
+                          void* stream, spmm_plan_t* plan_out);
+
+/*
+ * As spmm_csr_plan, with the kernel family forced (spmm_kernel value) and
+ * the merge-path range size set: items_per_cta = 0 picks the default,
+ * otherwise it must be a positive multiple of 256, at most 8192.
+ */
+spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
+                             int32_t kernel, int32_t items_per_cta, void* stream,
+                             spmm_plan_t* plan_out);
+
+/* Copy the plan's decisions into *info (host memory). */
+spmm_status spmm_plan_get_info(spmm_plan_t plan, spmm_plan_info* info);
+
+/* Free the plan and its workspace (synchronous). NULL is accepted. */
+spmm_status spmm_plan_destroy(spmm_plan_t plan);
+
+/*
+ * C = A . B with fp32 B, using a plan made for this A (same rowptr, M, nnz,
+ * N).  K is B's row count (colind values must lie in [0, K)).  Asynchronous
+ * on `stream`.  Returns SPMM_ERR_PLAN_MISMATCH for a NULL plan.
+ */
+spmm_status spmm_csr_f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind,
+                              const float* vals, const float* B, float* C, void* stream);
+
+/* As spmm_csr_f32_exec with B in bf16 (uint16 bit patterns), fp32 accumulate. */
+spmm_status spmm_csr_bf16f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind,
+                                  const float* vals, const uint16_t* B, float* C,
+                                  void* stream);
+
+/*
+ * One-call form: plans, multiplies and frees on `stream`.  Plan workspace is
+ * stream-ordered (cudaMallocAsync / cudaFreeAsync); the plan's statistics
+ * copy synchronises `stream` once.  For repeated products with the same A,
+ * build a plan once and call the _exec form.
+ */
+spmm_status spmm_csr_f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
+                         const int32_t* colind, const float* vals, const float* B, float* C,
+                         void* stream);
+
+/* One-call form with bf16 B (uint16 bit patterns), fp32 accumulate. */
+spmm_status spmm_csr_bf16f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
+                             const int32_t* colind, const float* vals, const uint16_t* B,
+                             float* C, void* stream);
+
+/*
+ * Check a CSR structure on the device: rowptr[0] = 0, rowptr non-decreasing,
+ * rowptr[M] = nnz, every colind in [0, K).  Synchronous (waits for
+ * `stream`).  Returns SPMM_OK or SPMM_ERR_INVALID_CSR.  Uses a 4-byte
+ * stream-ordered device allocation.
+ */
+spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int32_t M,
+                              int32_t K, int64_t nnz, void* stream);
+
+/*
+ * Synchronise `stream`, read and clear the plan's device error word.
+ * Returns SPMM_ERR_DEVICE_TIMEOUT if a kernel run with this plan gave up a
+ * bounded wait since the last check, else SPMM_OK.
+ */
+spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream);
+
+/*
+ * Optional timing hook.  When `event` (a cudaEvent_t passed as void*) is not
+ * NULL, every later exec with this plan records it on the exec stream right
+ * after the main SpMM kernel, before the balanced family's fixup kernel, so
+ * the main kernel can be timed alone with events.  NULL clears the hook.  The
+ * caller owns the event and keeps it alive while it is set.
+ */
+spmm_status spmm_plan_set_split_event(spmm_plan_t plan, void* event);
+
+/* Static, human-readable name of a status code. */
+const char* spmm_status_string(spmm_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSR_SPMM_02_GB300_SPMM_H_ */

@@ -1,0 +1,70 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+symbol include/spmm.h declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from csr_spmm_02_gb300 import spmm
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "spmm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return spmm.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(spmm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(spmm.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in spmm.STATUS_NAMES.items():
+        assert spmm.spmm_status_string(code) == name
+    assert spmm.spmm_status_string(99) == "SPMM_ERR_UNKNOWN"
+
+
+def test_argument_errors_without_cuda(lib):
+    out = ctypes.c_void_p()
+    null = ctypes.c_void_p()
+    # negative sizes, NULL output, bad option values: INVALID_ARG
+    assert lib.spmm_csr_plan(null, -1, 0, 4, null, ctypes.byref(out)) == 1
+    assert lib.spmm_csr_plan(null, 4, 0, -1, null, ctypes.byref(out)) == 1
+    assert lib.spmm_csr_plan(null, 4, 0, 4, null, None) == 1
+    assert lib.spmm_csr_plan(null, 4, 0, 4, null, ctypes.byref(out)) == 1  # NULL rowptr with M > 0
+    assert lib.spmm_csr_plan_ex(ctypes.c_void_p(16), 4, 0, 4, 7, 0, null, ctypes.byref(out)) == 1
+    assert lib.spmm_csr_plan_ex(ctypes.c_void_p(16), 4, 0, 4, 0, 300, null, ctypes.byref(out)) == 1
+    # nnz beyond int32: UNSUPPORTED
+    assert lib.spmm_csr_plan(ctypes.c_void_p(16), 4, 1 << 31, 4, null, ctypes.byref(out)) == 3
+    # exec without a plan: PLAN_MISMATCH
+    assert lib.spmm_csr_f32_exec(null, 4, null, null, null, null, null) == 4
+    assert lib.spmm_csr_bf16f32_exec(null, 4, null, null, null, null, null) == 4
+    # one-call forms: negative sizes rejected, M = 0 or N = 0 is a no-op success
+    assert lib.spmm_csr_f32(-1, 4, 4, null, null, null, null, null, null) == 1
+    assert lib.spmm_csr_f32(0, 4, 4, null, null, null, null, null, null) == 0
+    assert lib.spmm_csr_bf16f32(4, 4, 0, null, null, null, null, null, null) == 0
+    assert lib.spmm_csr_validate(null, null, 4, 4, 0, null) == 1
+    assert lib.spmm_csr_validate(ctypes.c_void_p(16), null, -1, 4, 0, null) == 1
+    assert lib.spmm_plan_destroy(null) == 0
+    assert lib.spmm_plan_check_device(null, null) == 1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        spmm.spmm_csr_plan(torch.zeros(5, dtype=torch.int32), 4, 0, 8)
