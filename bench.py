@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""SpMM benchmark: GFLOP/s (2*nnz*N / time) and effective HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step is one C = A . B over one of the seeded synthetic workloads
+(default ``uniform64k``: M=K=65536, 32 random columns per row, N=64, fp32),
+through the C ABI with a plan built once before timing (the plan is the
+per-structure preprocessing; its time is reported as ``config.plan_ms``).
+Inputs are resident in HBM before the timed region; L2 is flushed before every
+timed step by writing a 512 MiB buffer, and each step is timed with CUDA
+events on the launch stream.  Under torchrun every rank runs its own replica
+of the workload (independent problems, no data-path collective): ``value`` is
+the total work of all ranks divided by the slowest rank's time.
+
+Extra keys: ``roofline`` (the dominant kernel, timed alone through the plan's
+split event, against the measured HBM copy bandwidth), ``cpu_baseline`` (the
+CPU oracle on a bounded sample, one core), ``e2e`` (the one-call API with
+pinned host buffers, copies included), ``clocks`` (sampled during the timed
+region) and ``gpu_launches``.
+
+``--impl reference`` times the CPU oracle (the slow, plain fp64 row loop the
+tests check against) on the host cores, on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SpMM GFLOP/s (2*nnz*N/s) and effective HBM GB/s vs peak, 1xGB300"
+UNIT = "GFLOP/s"
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+# ----------------------------------------------------------------------------
+# distributed helpers (also exercised by the gloo tests)
+# ----------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def whole_job_rate(local_work: float, local_seconds: float) -> tuple[float, float]:
+    """(total work of all ranks / slowest rank's seconds, slowest seconds)."""
+    slowest = reduce_max(local_seconds)
+    total = reduce_sum(local_work)
+    return total / slowest, slowest
+
+
+# ----------------------------------------------------------------------------
+# measurement helpers
+# ----------------------------------------------------------------------------
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "csr_spmm_02_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu capture,
+    or None when there is none or the kernel sources changed since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)["captures"][workload][kernel]
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        self.index = ids[device_index] if device_index < len(ids) else str(device_index)
+        self.proc = None
+        self.error = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 "-i", self.index, "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:  # no nvidia-smi
+            self.error = str(e)
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": self.error or "nvidia-smi unavailable"}
+        time.sleep(0.05)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[3:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"error": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the CPU baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_rows_block(p, start, count):
+    import numpy as np
+    return np.arange(start, start + count, dtype=np.int32)
+
+
+def time_oracle(p, seconds: float):
+    """Run the oracle over consecutive row blocks (wrapping) for ~`seconds`.
+
+    Returns (GFLOP/s, description of the sample)."""
+    import numpy as np
+    import oracle
+    lens = np.diff(p.rowptr.astype(np.int64))
+    block = max(1, min(p.M, int(4e7 / max(1.0, lens.mean() * p.N))))  # ~4e7 multiply-adds per call
+    flops = 0.0
+    spent = 0.0
+    start = 0
+    rows_done = 0
+    while spent < seconds:
+        count = min(block, p.M - start)
+        rows = oracle_rows_block(p, start, count)
+        t0 = time.perf_counter()
+        oracle.spmm_reference(p.rowptr, p.colind, p.vals, p.B, b_dtype=p.b_dtype, rows=rows, with_bound=False)
+        spent += time.perf_counter() - t0
+        flops += 2.0 * float(lens[start:start + count].sum()) * p.N
+        rows_done += count
+        start = (start + count) % p.M
+    desc = (f"oracle over {rows_done} rows (consecutive blocks of {block} rows from row 0, wrapping; "
+            f"{flops / 2 / p.N:.0f} nonzeros x N={p.N}) in {spent:.2f} s, single thread")
+    return flops / spent / 1e9, desc
+
+
+def reference_arm(args, p, cfg):
+    """--impl reference: the CPU oracle, K timed steps of a bounded sample each."""
+    import numpy as np
+    import oracle
+    lens = np.diff(p.rowptr.astype(np.int64))
+    total_fma = float(lens.sum()) * p.N
+    if total_fma <= 4e8:
+        rows = None  # the whole workload per step
+        step_rows = p.M
+        step_flops = 2.0 * total_fma
+        sample = "whole workload per step"
+    else:
+        cum = np.cumsum(lens) * p.N
+        step_rows = int(np.searchsorted(cum, 2e8)) + 1
+        rows = np.arange(step_rows, dtype=np.int32)
+        step_flops = 2.0 * float(lens[:step_rows].sum()) * p.N
+        sample = f"rows 0..{step_rows - 1} per step ({step_flops / 2 / p.N:.0f} nonzeros x N={p.N})"
+    steps = args.steps if args.steps is not None else 10
+    for _ in range(args.warmup):
+        oracle.spmm_reference(p.rowptr, p.colind, p.vals, p.B, b_dtype=p.b_dtype, rows=rows, with_bound=False)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.spmm_reference(p.rowptr, p.colind, p.vals, p.B, b_dtype=p.b_dtype, rows=rows, with_bound=False)
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = step_flops / sec / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def gpu_arm(args, p, cfg, ws, rank, local):
+    import numpy as np
+    import torch
+    from csr_spmm_02_gb300 import spmm
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    bf16 = p.b_dtype == "bf16"
+    B_host = p.B.view(np.int16) if bf16 else p.B
+    rowptr = torch.from_numpy(p.rowptr).to(dev)
+    colind = torch.from_numpy(p.colind).to(dev)
+    vals = torch.from_numpy(p.vals).to(dev)
+    B = torch.from_numpy(np.ascontiguousarray(B_host)).to(dev)
+    C = torch.empty((p.M, p.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    plan = spmm.spmm_csr_plan(rowptr, p.M, p.nnz, p.N, kernel=args.kernel, items_per_cta=args.items_per_cta)
+    torch.cuda.synchronize()
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    info = plan.info()
+    run = spmm.spmm_csr_bf16f32_exec if bf16 else spmm.spmm_csr_f32_exec
+    launches_per_step = 1 if info["kernel"] == "row" else 2
+
+    def step():
+        run(plan, p.K, colind, vals, B, C)
+
+    for i in range(max(args.warmup, 0)):
+        flush.fill_(float(i))
+        step()
+    torch.cuda.synchronize()
+    steps = args.steps
+    if steps is None:  # aim for ~1.5 s of timed region
+        t0 = time.perf_counter()
+        for i in range(5):
+            flush.fill_(float(i))
+            step()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 5
+        steps = int(min(20000, max(50, 1.5 / max(per, 1e-6))))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    splits = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in splits:
+        e.record()  # create the events before the timed region
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.1)
+    for i in range(steps):
+        flush.fill_(float(i))
+        spmm.spmm_plan_set_split_event(plan, splits[i])
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    spmm.spmm_plan_set_split_event(plan, None)
+    assert spmm.spmm_plan_check_device(plan) == 0, "device error word set"
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    main_ms = [s.elapsed_time(m) for s, m in zip(starts, splits)]
+    local_sec = sum(step_ms) / 1e3
+    value_flops, slowest = whole_job_rate(float(p.flops()) * steps, local_sec)
+    ms_per_step = slowest / steps * 1e3
+    peak, peak_kind = measured_hbm_peak()
+    mean_main = sum(main_ms) / len(main_ms)
+    achieved = p.compulsory_bytes() / (mean_main * 1e-3) / 1e9
+    traffic = ncu_traffic(p.name, info["kernel"])
+    eff_gbs = p.compulsory_bytes() / (ms_per_step * 1e-3) / 1e9 * 1.0
+
+    # end to end: pinned host inputs -> device, one-call API, C -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        h = {"rowptr": torch.from_numpy(p.rowptr).pin_memory(), "colind": torch.from_numpy(p.colind).pin_memory(),
+             "vals": torch.from_numpy(p.vals).pin_memory(),
+             "B": torch.from_numpy(np.ascontiguousarray(B_host)).pin_memory()}
+        d = {"rowptr": rowptr, "colind": colind, "vals": vals, "B": B}
+        C_host = torch.empty((p.M, p.N), dtype=torch.float32).pin_memory()
+        one_call = spmm.spmm_csr_bf16f32 if bf16 else spmm.spmm_csr_f32
+        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        d2h = C_host.numel() * 4
+
+        def e2e_step():
+            for k in h:
+                d[k].copy_(h[k], non_blocking=True)
+            one_call(p.M, p.K, p.N, d["rowptr"], d["colind"], d["vals"], d["B"], C)
+            C_host.copy_(C, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        n_e2e = max(3, min(steps, 20))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_sec = time.perf_counter() - t0
+        e2e_rate, _ = whole_job_rate(float(p.flops()) * n_e2e, e2e_sec)
+        e2e = {"value": e2e_rate / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": n_e2e, "api": "spmm_csr_bf16f32" if bf16 else "spmm_csr_f32"}
+
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        val, desc = time_oracle(p, args.cpu_seconds)
+        cpu = {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+
+    cfg = dict(cfg)
+    cfg.update({"kernel": info["kernel"], "items_per_cta": info["items_per_cta"], "num_ctas": info["num_ctas"],
+                "plan_ms": round(plan_ms, 3), "max_row_nnz": info["max_row_nnz"],
+                "l2": f"flushed before every timed step (write of {FLUSH_BYTES >> 20} MiB)",
+                "timing": "CUDA events per step on the launch stream; plan built once before timing"})
+    line = {
+        "metric": METRIC, "value": value_flops / 1e9, "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy PCG64)", "config": cfg,
+        "effective_hbm_gbs": eff_gbs, "effective_hbm_frac": eff_gbs / peak,
+        "gflops_best": p.flops() / (min(step_ms) * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": info["kernel"], "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes": p.compulsory_bytes(),
+                     "kernel_ms": mean_main},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": steps * launches_per_step,
+    }
+    plan.destroy()
+    return line
+
+
+def main(argv=None):
+    from csr_spmm_02_gb300 import gen
+
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=gen.WORKLOAD_ORDER, default="uniform64k")
+    ap.add_argument("--kernel", choices=["auto", "row", "balanced"], default="auto")
+    ap.add_argument("--items-per-cta", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+
+    ws, rank, local = dist_env()
+    if args.impl == "reference" and rank != 0:
+        return 0  # rank 0 alone times the CPU oracle
+    p = gen.make_workload(args.workload)
+    cfg = {"workload": args.workload, "M": p.M, "K": p.K, "N": p.N, "nnz": p.nnz, "b_dtype": p.b_dtype,
+           "seed": p.seed, "compulsory_bytes": p.compulsory_bytes()}
+    if args.impl == "reference":
+        print(json.dumps(reference_arm(args, p, cfg)), flush=True)
+        return 0
+
+    import __graft_entry__
+    __graft_entry__.build()
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = gpu_arm(args, p, cfg, ws, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,4 +1,5 @@
 // C ABI entry points: exec with a plan, the one-call forms, status strings.
+#include <algorithm>
 #include <cstdint>
 
 #include "spmm_internal.h"
@@ -17,12 +18,13 @@ static int pow2_at_least(int x) {
 }
 
 Shape choose_shape(int32_t N, bool bf16, bool vector_ok) {
-  const int vec = bf16 ? 8 : 4;
   if (vector_ok) {
-    const int lanes = N / vec;  // N is a multiple of vec here
-    if (lanes <= 32) return Shape{vec, pow2_at_least(lanes), 1};
-    if (lanes <= 64) return Shape{vec, 32, 2};
-    return Shape{vec, 32, bf16 ? 2 : 4};  // wider N runs as several column tiles
+    const int vec = bf16 ? 8 : 4;
+    const int chunks = bf16 ? SPMM_BF16_CHUNKS : SPMM_LANE_CHUNKS;
+    const int L = N / vec;  // 16-byte vectors per row (N is a multiple of vec here)
+    if (L <= chunks) return Shape{vec, 1, pow2_at_least(L)};
+    // G lanes of `chunks` vectors each; rows wider than 32 lanes run as column tiles
+    return Shape{vec, std::min(32, pow2_at_least((L + chunks - 1) / chunks)), chunks};
   }
   return N <= 8 ? Shape{1, 8, 1} : Shape{1, 32, 1};
 }

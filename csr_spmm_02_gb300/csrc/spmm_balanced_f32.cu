@@ -6,8 +6,8 @@ namespace spmm {
 cudaError_t launch_balanced_f32(const Launch& L, Shape s) {
 #define X(V, GG, NC) \
   if (s.vec == V && s.G == GG && s.nch == NC) return launch_balanced_t<float, V, GG, NC>(L);
-  X(4, 1, 1) X(4, 2, 1) X(4, 4, 1) X(4, 8, 1) X(4, 16, 1) X(4, 32, 1) X(4, 32, 2)
-  X(1, 8, 1) X(1, 32, 1) X(4, 32, 4)
+  SPMM_VECTOR_SHAPES(X, 4, SPMM_LANE_CHUNKS)
+  SPMM_SCALAR_SHAPES(X)
 #undef X
   return cudaErrorInvalidConfiguration;
 }

@@ -18,6 +18,43 @@ namespace spmm {
 constexpr int kThreads = 256;           // threads per CTA for every SpMM kernel
 constexpr uint32_t kSpinLimit = 1u << 22;  // bound on mbarrier polls before giving up
 
+#ifndef SPMM_L2_HINTS
+#define SPMM_L2_HINTS 1  // stream A and C with evict-first so B's reused rows stay in L2
+#endif
+#ifndef SPMM_B_EVICT_LAST
+#define SPMM_B_EVICT_LAST 0  // give B gathers evict-last priority in L2
+#endif
+
+// ---------------------------------------------------------------------------
+// L2 cache policies.  A (colind, vals, rowptr) is read once and C is written
+// once: both are marked evict-first, so the L2 keeps the rows of B that many
+// nonzeros reuse (the temporal locality the kkmem page attributes to B).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Read-once loads of A's arrays.
+__device__ __forceinline__ int ld_stream(const int* p, uint64_t pol) {
+#if SPMM_L2_HINTS
+  int v;
+  asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+  return v;
+#else
+  return __ldg(p);
+#endif
+}
+__device__ __forceinline__ float ld_stream(const float* p, uint64_t pol) {
+  return __int_as_float(ld_stream(reinterpret_cast<const int*>(p), pol));
+}
+
 // ---------------------------------------------------------------------------
 // B slices
 // ---------------------------------------------------------------------------
@@ -28,6 +65,16 @@ template <>
 struct BSlice<float, 4> {
   float4 r;
   __device__ __forceinline__ void load(const float* p) { r = __ldg(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ void load_if(const float* p, bool pred) {
+#if SPMM_B_EVICT_LAST
+    r = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (pred)
+      asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+                   : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p), "l"(policy_evict_last()));
+#else
+    r = pred ? __ldg(reinterpret_cast<const float4*>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#endif
+  }
   __device__ __forceinline__ void widen(float (&o)[4]) const {
     o[0] = r.x; o[1] = r.y; o[2] = r.z; o[3] = r.w;
   }
@@ -37,6 +84,7 @@ template <>
 struct BSlice<float, 1> {
   float r;
   __device__ __forceinline__ void load(const float* p) { r = __ldg(p); }
+  __device__ __forceinline__ void load_if(const float* p, bool pred) { r = pred ? __ldg(p) : 0.f; }
   __device__ __forceinline__ void widen(float (&o)[1]) const { o[0] = r; }
 };
 
@@ -47,6 +95,16 @@ template <>
 struct BSlice<uint16_t, 8> {
   uint4 r;
   __device__ __forceinline__ void load(const uint16_t* p) { r = __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ __forceinline__ void load_if(const uint16_t* p, bool pred) {
+#if SPMM_B_EVICT_LAST
+    r = make_uint4(0u, 0u, 0u, 0u);
+    if (pred)
+      asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                   : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p), "l"(policy_evict_last()));
+#else
+    r = pred ? __ldg(reinterpret_cast<const uint4*>(p)) : make_uint4(0u, 0u, 0u, 0u);
+#endif
+  }
   __device__ __forceinline__ void widen(float (&o)[8]) const {
     o[0] = bf16_lo(r.x); o[1] = bf16_hi(r.x);
     o[2] = bf16_lo(r.y); o[3] = bf16_hi(r.y);
@@ -61,28 +119,37 @@ struct BSlice<uint16_t, 1> {
   __device__ __forceinline__ void load(const uint16_t* p) {
     r = __ldg(reinterpret_cast<const unsigned short*>(p));
   }
+  __device__ __forceinline__ void load_if(const uint16_t* p, bool pred) {
+    r = pred ? __ldg(reinterpret_cast<const unsigned short*>(p)) : (unsigned short)0;
+  }
   __device__ __forceinline__ void widen(float (&o)[1]) const { o[0] = __uint_as_float(uint32_t(r) << 16); }
 };
 
 // ---------------------------------------------------------------------------
-// acc += v * b
+// acc += v * b.  The scalar v is packed once per nonzero into a (v, v) pair
+// that every packed FMA of that nonzero reuses.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void fma2(float& a0, float& a1, float v, float b0, float b1) {
-  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-      "mov.b64 ra, {%2, %2};\n\t"
+__device__ __forceinline__ uint64_t pack_pair(float v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ void fma2(float& a0, float& a1, uint64_t vv, float b0, float b1) {
+  asm("{\n\t.reg .b64 rb, rc;\n\t"
       "mov.b64 rb, {%3, %4};\n\t"
       "mov.b64 rc, {%0, %1};\n\t"
-      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "fma.rn.f32x2 rc, %2, rb, rc;\n\t"
       "mov.b64 {%0, %1}, rc;\n\t}"
       : "+f"(a0), "+f"(a1)
-      : "f"(v), "f"(b0), "f"(b1));
+      : "l"(vv), "f"(b0), "f"(b1));
 }
 
 template <int VEC>
-__device__ __forceinline__ void axpy(float (&acc)[VEC], float v, const float (&b)[VEC]) {
+__device__ __forceinline__ void axpy(float (&acc)[VEC], float v, uint64_t vv, const float (&b)[VEC]) {
   if constexpr (VEC % 2 == 0) {
 #pragma unroll
-    for (int j = 0; j < VEC; j += 2) fma2(acc[j], acc[j + 1], v, b[j], b[j + 1]);
+    for (int j = 0; j < VEC; j += 2) fma2(acc[j], acc[j + 1], vv, b[j], b[j + 1]);
   } else {
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = fmaf(v, b[j], acc[j]);
@@ -92,16 +159,31 @@ __device__ __forceinline__ void axpy(float (&acc)[VEC], float v, const float (&b
 // ---------------------------------------------------------------------------
 // C stores (each C element is written once: streaming / evict-first)
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void st_stream4(float* p, float x, float y, float z, float w) {
+#if SPMM_L2_HINTS
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "f"(x), "f"(y), "f"(z), "f"(w),
+               "l"(policy_evict_first())
+               : "memory");
+#else
+  __stcs(reinterpret_cast<float4*>(p), make_float4(x, y, z, w));
+#endif
+}
+__device__ __forceinline__ void st_stream1(float* p, float x) {
+#if SPMM_L2_HINTS
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(x), "l"(policy_evict_first()) : "memory");
+#else
+  __stcs(p, x);
+#endif
+}
+
 template <int VEC>
 __device__ __forceinline__ void store_c(float* p, const float (&a)[VEC]) {
-  if constexpr (VEC == 4) {
-    __stcs(reinterpret_cast<float4*>(p), make_float4(a[0], a[1], a[2], a[3]));
-  } else if constexpr (VEC == 8) {
-    __stcs(reinterpret_cast<float4*>(p), make_float4(a[0], a[1], a[2], a[3]));
-    __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(a[4], a[5], a[6], a[7]));
+  if constexpr (VEC % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < VEC; j += 4) st_stream4(p + j, a[j], a[j + 1], a[j + 2], a[j + 3]);
   } else {
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) __stcs(p + j, a[j]);
+    for (int j = 0; j < VEC; ++j) st_stream1(p + j, a[j]);
   }
 }
 
@@ -149,10 +231,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 // dst (shared) and src (global) 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+#if SPMM_L2_HINTS
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy_evict_first())
+      : "memory");
+#else
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+#endif
 }
 
 // Poll the barrier's phase `parity` at most `limit` times; true when it completed.

@@ -65,6 +65,20 @@ cudaError_t launch_balanced_bf16(const Launch& L, Shape s);
 cudaError_t launch_fixup(const Launch& L);
 
 
+// 16-byte chunks of the output row each lane owns (fp32: 4 columns per chunk;
+// bf16 B: 8 columns per chunk, so half as many chunks).  Wider lane slices
+// spread each nonzero's bookkeeping over fewer lanes.
+#ifndef SPMM_LANE_CHUNKS
+#define SPMM_LANE_CHUNKS 1
+#endif
+#define SPMM_BF16_CHUNKS (SPMM_LANE_CHUNKS / 2 > 0 ? SPMM_LANE_CHUNKS / 2 : 1)
+
+// (VEC, G, NCH) shapes compiled for each kernel: small rows use one lane with
+// 1, 2 or 4 chunks; wider rows use G lanes with the standard chunk count.
+#define SPMM_VECTOR_SHAPES(X, V, NC)                                                            \
+  X(V, 1, 1) X(V, 1, 2) X(V, 1, 4) X(V, 2, NC) X(V, 4, NC) X(V, 8, NC) X(V, 16, NC) X(V, 32, NC)
+#define SPMM_SCALAR_SHAPES(X) X(1, 8, 1) X(1, 32, 1)
+
 constexpr int kDefaultItemsPerCta = 2048;
 constexpr int kMaxItemsPerCta = 8192;
 constexpr int kMaxDevices = 64;

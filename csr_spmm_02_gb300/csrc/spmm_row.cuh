@@ -10,43 +10,61 @@
 // point): each lane owns NCH chunks of VEC consecutive columns, so every B
 // gather is one 16-byte load per lane, coalesced across the group.
 //
-// Per chunk of G nonzeros the group loads G (colind, vals) pairs with one
-// coalesced load per lane and broadcasts them with warp shuffles; U B-row
-// gathers are issued before the FMAs that consume them, so each lane keeps U
-// 16-byte loads in flight.  Rows are summed in index order by one group, so
-// results are deterministic.  C rows are stored once with streaming stores.
+// A group stages a chunk of its row's (colind, vals) pairs in shared memory
+// with coalesced loads; every lane then reads each pair with a broadcast
+// shared load.  U gathers of B rows are issued before the FMAs that consume
+// them; a short last batch is zero-extended (it re-reads a valid row and adds
+// it with value 0, the zero extension the Sgap page describes), so the inner
+// loop has no branches.  Each lane owns NCH 16-byte chunks, so the per-nonzero
+// bookkeeping (shared loads, address arithmetic) is paid by few lanes for
+// many columns.  The summation order is fixed, so results are deterministic.
 #pragma once
 
 #include "spmm_device.cuh"
 #include "spmm_internal.h"
 
+#ifndef SPMM_ROW_LOADS
+#define SPMM_ROW_LOADS 4  // 16-byte B loads in flight per lane (U nonzeros x NCH chunks)
+#endif
+#ifndef SPMM_ROW_MIN_BLOCKS
+#define SPMM_ROW_MIN_BLOCKS 1
+#endif
+
 namespace spmm {
 
 template <int G, int NCH>
-struct RowUnroll {
-  static constexpr int kBase = NCH >= 4 ? 2 : (NCH == 2 ? 4 : 8);
-  static constexpr int value = kBase < G ? kBase : G;
+struct RowTiling {
+  static constexpr int kChunk = G > 16 ? G : 16;  // (col, val) pairs a group stages at a time
+  static constexpr int kU0 = SPMM_ROW_LOADS / NCH > 0 ? SPMM_ROW_LOADS / NCH : 1;
+  static constexpr int U = kU0 < kChunk ? kU0 : kChunk;  // nonzeros per batch; divides kChunk
 };
 
 template <typename BT, int VEC, int G, int NCH>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, SPMM_ROW_MIN_BLOCKS)
     spmm_row_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr,
                     const int32_t* __restrict__ colind, const float* __restrict__ vals,
                     const BT* __restrict__ B, float* __restrict__ C) {
   constexpr int kGroups = kThreads / G;
-  constexpr int U = RowUnroll<G, NCH>::value;
+  constexpr int CH = RowTiling<G, NCH>::kChunk;
+  constexpr int U = RowTiling<G, NCH>::U;
+  __shared__ int2 s_cv[kGroups * CH];  // group g stages (col, val bits) in s_cv[g*CH, g*CH+CH)
+
   const int lane = threadIdx.x & (G - 1);
-  const int64_t row = int64_t(blockIdx.x) * kGroups + threadIdx.x / G;
+  const int grp = threadIdx.x / G;
+  const int64_t row = int64_t(blockIdx.x) * kGroups + grp;
   if (row >= M) return;  // the whole group leaves together
   const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << ((threadIdx.x & 31) & ~(G - 1)));
+  int2* cv = s_cv + grp * CH;
 
+  // Columns of this lane: NCH chunks of VEC, chunk ch at col0 + (ch*G + lane)*VEC.
+  // Loads use offsets clamped into the row (a lane past N re-reads a valid
+  // slice it never stores), so the inner loop needs no column predicate.
   const int col0 = blockIdx.y * (G * VEC * NCH);
-  int coff[NCH];
-  bool cok[NCH];
+  int coff[NCH], coffl[NCH];
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
     coff[ch] = col0 + (ch * G + lane) * VEC;
-    cok[ch] = coff[ch] < N;
+    coffl[ch] = min(coff[ch], N - VEC);
   }
   float acc[NCH][VEC];
 #pragma unroll
@@ -54,42 +72,35 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[ch][j] = 0.f;
 
-  const int start = __ldg(rowptr + row);
-  const int end = __ldg(rowptr + row + 1);
-  for (int base = start; base < end; base += G) {
-    const int cnt = min(G, end - base);
-    int my_c = 0;
-    float my_v = 0.f;
-    if (lane < cnt) {
-      my_c = __ldg(colind + base + lane);
-      my_v = __ldg(vals + base + lane);
-    }
+  const uint64_t stream_pol = policy_evict_first();
+  const int start = ld_stream(rowptr + row, stream_pol);
+  const int end = ld_stream(rowptr + row + 1, stream_pol);
+  for (int base = start; base < end; base += CH) {
+    const int cnt = min(CH, end - base);
+    __syncwarp(gmask);  // every lane has finished with the previous chunk
+    for (int j = lane; j < cnt; j += G)
+      cv[j] = make_int2(ld_stream(colind + base + j, stream_pol),
+                        ld_stream(reinterpret_cast<const int*>(vals) + base + j, stream_pol));
+    __syncwarp(gmask);
     for (int t = 0; t < cnt; t += U) {
+      // Gathers first (a padded slot re-reads the chunk's last row); values
+      // are re-read from shared memory afterwards to keep registers for loads.
       BSlice<BT, VEC> bs[U][NCH];
-      float v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int src = (t + u) & (G - 1);
-        const int c = __shfl_sync(gmask, my_c, src, G);
-        v[u] = __shfl_sync(gmask, my_v, src, G);
-        if (t + u < cnt) {
-          const BT* brow = B + size_t(c) * N;
+        const BT* brow = B + size_t(cv[min(t + u, cnt - 1)].x) * N;
 #pragma unroll
-          for (int ch = 0; ch < NCH; ++ch)
-            if (cok[ch]) bs[u][ch].load(brow + coff[ch]);
-        }
+        for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(brow + coffl[ch]);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (t + u < cnt) {
+        const float v = t + u < cnt ? __int_as_float(cv[t + u].y) : 0.f;  // padded slot adds 0
+        const uint64_t vv = pack_pair(v);
 #pragma unroll
-          for (int ch = 0; ch < NCH; ++ch) {
-            if (cok[ch]) {
-              float b[VEC];
-              bs[u][ch].widen(b);
-              axpy<VEC>(acc[ch], v[u], b);
-            }
-          }
+        for (int ch = 0; ch < NCH; ++ch) {
+          float b[VEC];
+          bs[u][ch].widen(b);
+          axpy<VEC>(acc[ch], v, vv, b);
         }
       }
     }
@@ -97,7 +108,7 @@ __global__ void __launch_bounds__(kThreads)
   float* crow = C + size_t(row) * N;
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch)
-    if (cok[ch]) store_c<VEC>(crow + coff[ch], acc[ch]);
+    if (coff[ch] < N) store_c<VEC>(crow + coff[ch], acc[ch]);
 }
 
 template <typename BT, int VEC, int G, int NCH>

@@ -202,7 +202,8 @@ def spmm_plan_set_split_event(plan: Plan, event) -> None:
     """Record `event` (a torch.cuda.Event, or None) after the main kernel of every exec."""
     handle = None
     if event is not None:
-        event.record()  # make sure the event exists before handing its handle over
+        if not event.cuda_event:
+            event.record()  # torch creates the CUDA event on its first record
         handle = ctypes.c_void_p(event.cuda_event)
     plan._split_event = event  # keep it alive while it is set
     _check(load().spmm_plan_set_split_event(plan.handle, handle), "spmm_plan_set_split_event")

@@ -55,6 +55,14 @@
 
 #include <stdint.h>
 
+/* Only the functions below are exported; everything else in the library is
+ * hidden (it is built with -fvisibility=hidden). */
+#if defined(__GNUC__)
+#define SPMM_API __attribute__((visibility("default")))
+#else
+#define SPMM_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -104,7 +112,7 @@ typedef struct {
  * EB scheme of its DA-SpMM design space).  The plan's workspace is
  * allocated with cudaMalloc.  *plan_out receives the plan (NULL on error).
  */
-spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
+SPMM_API spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
                           void* stream, spmm_plan_t* plan_out);
 
 /*
@@ -112,26 +120,26 @@ spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t
  * the merge-path range size set: items_per_cta = 0 picks the default,
  * otherwise it must be a positive multiple of 256, at most 8192.
  */
-spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
+SPMM_API spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
                              int32_t kernel, int32_t items_per_cta, void* stream,
                              spmm_plan_t* plan_out);
 
 /* Copy the plan's decisions into *info (host memory). */
-spmm_status spmm_plan_get_info(spmm_plan_t plan, spmm_plan_info* info);
+SPMM_API spmm_status spmm_plan_get_info(spmm_plan_t plan, spmm_plan_info* info);
 
 /* Free the plan and its workspace (synchronous). NULL is accepted. */
-spmm_status spmm_plan_destroy(spmm_plan_t plan);
+SPMM_API spmm_status spmm_plan_destroy(spmm_plan_t plan);
 
 /*
  * C = A . B with fp32 B, using a plan made for this A (same rowptr, M, nnz,
  * N).  K is B's row count (colind values must lie in [0, K)).  Asynchronous
  * on `stream`.  Returns SPMM_ERR_PLAN_MISMATCH for a NULL plan.
  */
-spmm_status spmm_csr_f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind,
+SPMM_API spmm_status spmm_csr_f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind,
                               const float* vals, const float* B, float* C, void* stream);
 
 /* As spmm_csr_f32_exec with B in bf16 (uint16 bit patterns), fp32 accumulate. */
-spmm_status spmm_csr_bf16f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind,
+SPMM_API spmm_status spmm_csr_bf16f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind,
                                   const float* vals, const uint16_t* B, float* C,
                                   void* stream);
 
@@ -141,12 +149,12 @@ spmm_status spmm_csr_bf16f32_exec(spmm_plan_t plan, int32_t K, const int32_t* co
  * copy synchronises `stream` once.  For repeated products with the same A,
  * build a plan once and call the _exec form.
  */
-spmm_status spmm_csr_f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
+SPMM_API spmm_status spmm_csr_f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
                          const int32_t* colind, const float* vals, const float* B, float* C,
                          void* stream);
 
 /* One-call form with bf16 B (uint16 bit patterns), fp32 accumulate. */
-spmm_status spmm_csr_bf16f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
+SPMM_API spmm_status spmm_csr_bf16f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
                              const int32_t* colind, const float* vals, const uint16_t* B,
                              float* C, void* stream);
 
@@ -156,7 +164,7 @@ spmm_status spmm_csr_bf16f32(int32_t M, int32_t K, int32_t N, const int32_t* row
  * `stream`).  Returns SPMM_OK or SPMM_ERR_INVALID_CSR.  Uses a 4-byte
  * stream-ordered device allocation.
  */
-spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int32_t M,
+SPMM_API spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int32_t M,
                               int32_t K, int64_t nnz, void* stream);
 
 /*
@@ -164,7 +172,7 @@ spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int3
  * Returns SPMM_ERR_DEVICE_TIMEOUT if a kernel run with this plan gave up a
  * bounded wait since the last check, else SPMM_OK.
  */
-spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream);
+SPMM_API spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream);
 
 /*
  * Optional timing hook.  When `event` (a cudaEvent_t passed as void*) is not
@@ -173,10 +181,10 @@ spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream);
  * the main kernel can be timed alone with events.  NULL clears the hook.  The
  * caller owns the event and keeps it alive while it is set.
  */
-spmm_status spmm_plan_set_split_event(spmm_plan_t plan, void* event);
+SPMM_API spmm_status spmm_plan_set_split_event(spmm_plan_t plan, void* event);
 
 /* Static, human-readable name of a status code. */
-const char* spmm_status_string(spmm_status status);
+SPMM_API const char* spmm_status_string(spmm_status status);
 
 #ifdef __cplusplus
 }
