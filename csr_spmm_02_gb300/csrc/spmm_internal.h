@@ -63,6 +63,9 @@ cudaError_t launch_row_bf16(const Launch& L, Shape s);
 cudaError_t launch_balanced_f32(const Launch& L, Shape s);
 cudaError_t launch_balanced_bf16(const Launch& L, Shape s);
 cudaError_t launch_fixup(const Launch& L);
+// Merge-path coordinates of the P+1 range starts (ranges of T items) into part.
+cudaError_t launch_partition(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t T, int32_t P, int2* part,
+                             cudaStream_t stream);
 
 
 // 16-byte chunks of the output row each lane owns (fp32: 4 columns per chunk;

@@ -1,0 +1,106 @@
+// One-call SpMM that allocates no memory.
+//
+// Some callers cannot call cudaMalloc or any other allocator at the moment
+// they need a product: code running inside a memory pool or arena that owns
+// all device memory, real-time loops where an allocation's implicit
+// synchronisation or failure is not acceptable, and embedders whose own
+// allocator must not be bypassed.  For them spmm_csr_f32_noalloc runs the
+// nnz-balanced path with its scratch (merge-path range coordinates, carry
+// rows of rows that cross ranges, the error word) carved from one
+// fixed-size array in the library's own device memory instead.
+//
+// The array is a file-scope static __device__ object, so every GPU that
+// loads the library holds it (kNoallocScratchBytes) until the process
+// exits.  Host code cannot use the array's name as a device address; the
+// first call on each device looks the address up with cudaGetSymbolAddress
+// while that device is current and remembers it.  All calls share the
+// array and each call overwrites it: calls that may overlap on the GPU
+// (different streams, or different host threads) race and must be ordered by
+// the caller.
+#include <cstdint>
+#include <mutex>
+
+#include "spmm_internal.h"
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = size_t(32) << 20;  // 32 MiB per device
+constexpr int kNoallocItemsPerCta = spmm::kDefaultItemsPerCta;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[spmm::kMaxDevices] = {};
+
+// Device address of the scratch array on `dev` (which must be current).
+cudaError_t noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= spmm::kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" SPMM_API spmm_status spmm_csr_f32_noalloc(int32_t M, int32_t K, int32_t N, int64_t nnz,
+                                                     const int32_t* rowptr, const int32_t* colind,
+                                                     const float* vals, const float* B, float* C, void* stream) {
+  using namespace spmm;
+  if (M < 0 || K < 0 || N < 0 || nnz < 0) return SPMM_ERR_INVALID_ARG;
+  if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return SPMM_OK;
+  if (!rowptr || !C || (nnz > 0 && (!colind || !vals || !B || K == 0))) return SPMM_ERR_INVALID_ARG;
+
+  // Scratch layout: [error word | range coordinates (P+1) | carry rows (P x 2 x N)].
+  const int64_t P = (int64_t(M) + nnz + kNoallocItemsPerCta - 1) / kNoallocItemsPerCta;
+  const size_t err_bytes = 256;
+  const size_t part_bytes = align256(size_t(P + 1) * sizeof(int2));
+  const size_t carry_bytes = size_t(P) * 2 * size_t(N) * sizeof(float);
+  if (P > INT32_MAX - 1 || err_bytes + part_bytes + carry_bytes > kNoallocScratchBytes)
+    return SPMM_ERR_UNSUPPORTED;  // the problem needs more scratch than the fixed array holds
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPMM_ERR_CUDA;
+  void* base = nullptr;
+  if (noalloc_scratch(dev, &base) != cudaSuccess) return SPMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* scratch = static_cast<unsigned char*>(base);
+  int* err = reinterpret_cast<int*>(scratch);
+  int2* part = reinterpret_cast<int2*>(scratch + err_bytes);
+  float* carry = reinterpret_cast<float*>(scratch + err_bytes + part_bytes);
+
+  // The array keeps the previous call's contents: only the error word must
+  // start at zero (ranges and carry rows are written before they are read).
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SPMM_ERR_CUDA;
+  if (launch_partition(rowptr, M, nnz, kNoallocItemsPerCta, int32_t(P), part, s) != cudaSuccess)
+    return SPMM_ERR_CUDA;
+
+  const bool vector_ok = N % 4 == 0 && (reinterpret_cast<uintptr_t>(B) & 15) == 0 &&
+                         (reinterpret_cast<uintptr_t>(C) & 15) == 0;
+  Launch L{};
+  L.M = M;
+  L.N = N;
+  L.nnz = nnz;
+  L.rowptr = rowptr;
+  L.colind = colind;
+  L.vals = vals;
+  L.B = B;
+  L.C = C;
+  L.part = part;
+  L.num_ctas = int32_t(P);
+  L.items_per_cta = kNoallocItemsPerCta;
+  L.carry = carry;
+  L.err = err;
+  L.stream = s;
+  cudaError_t e = launch_balanced_f32(L, choose_shape(N, false, vector_ok));
+  if (e == cudaSuccess) e = launch_fixup(L);
+  return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+}

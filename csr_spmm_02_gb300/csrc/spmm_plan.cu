@@ -100,6 +100,13 @@ cudaError_t launch_fixup(const Launch& L) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_partition(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t T, int32_t P, int2* part,
+                             cudaStream_t stream) {
+  const unsigned grid = unsigned((int64_t(P) + 1 + kThreads - 1) / kThreads);
+  merge_path_partition_kernel<<<grid, kThreads, 0, stream>>>(rowptr, M, nnz, T, P, part);
+  return cudaGetLastError();
+}
+
 }  // namespace spmm
 
 using namespace spmm;

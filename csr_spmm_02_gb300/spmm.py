@@ -37,7 +37,7 @@ KERNEL_NAMES = {1: "row", 2: "balanced"}
 EXPORTS = ["spmm_csr_plan", "spmm_csr_plan_ex", "spmm_plan_get_info", "spmm_plan_destroy",
            "spmm_csr_f32_exec", "spmm_csr_bf16f32_exec", "spmm_csr_f32", "spmm_csr_bf16f32",
            "spmm_csr_validate", "spmm_plan_check_device", "spmm_plan_set_split_event",
-           "spmm_status_string"]
+           "spmm_csr_f32_noalloc", "spmm_status_string"]
 
 
 class SpmmError(RuntimeError):
@@ -82,6 +82,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "spmm_csr_validate": [vp, vp, i32, i32, i64, vp],
         "spmm_plan_check_device": [vp, vp],
         "spmm_plan_set_split_event": [vp, vp],
+        "spmm_csr_f32_noalloc": [i32, i32, i32, i64, vp, vp, vp, vp, vp, vp],
         "spmm_status_string": [ctypes.c_int],
     }
     for name, args in sig.items():
@@ -182,6 +183,14 @@ def spmm_csr_bf16f32(M, K, N, rowptr, colind, vals, B, C, stream=None):
     _check(load().spmm_csr_bf16f32(M, K, N, _ptr(rowptr, _I32, "rowptr"), _ptr(colind, _I32, "colind", True),
                                    _ptr(vals, _F32, "vals", True), _ptr(B, _BF16_BITS, "B", True),
                                    _ptr(C, _F32, "C"), _stream(stream)), "spmm_csr_bf16f32")
+    return C
+
+
+def spmm_csr_f32_noalloc(M, K, N, nnz, rowptr, colind, vals, B, C, stream=None):
+    """C = A . B (fp32) with the library's fixed scratch array: no allocation anywhere."""
+    _check(load().spmm_csr_f32_noalloc(M, K, N, nnz, _ptr(rowptr, _I32, "rowptr"), _ptr(colind, _I32, "colind", True),
+                                       _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True), _ptr(C, _F32, "C"),
+                                       _stream(stream)), "spmm_csr_f32_noalloc")
     return C
 
 

@@ -175,6 +175,33 @@ SPMM_API spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* col
 SPMM_API spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream);
 
 /*
+ * C = A . B with fp32 B, allocating no memory at all (no cudaMalloc,
+ * cudaMallocAsync or allocating library call, here or in the kernels).  The
+ * pages this library follows have no counterpart to this call: it exists for
+ * callers that must not allocate while they multiply -- code inside a memory
+ * pool or arena that owns all device memory, real-time loops that cannot
+ * accept an allocation's synchronisation or failure, embedders whose own
+ * allocator must not be bypassed.
+ *
+ * It always runs the nnz-balanced kernel and its fixup, with their scratch
+ * (range coordinates, carry rows, error word) in one fixed 32 MiB array of
+ * device memory that the library itself holds on every device that loads it,
+ * until the process exits.  The caller passes all inputs and the output, as
+ * for spmm_csr_f32, plus nnz (which must equal rowptr[M]).  A problem whose
+ * scratch, about 8 * (P + 1) + 8 * N * P bytes with P = ceil((M + nnz) / 2048),
+ * exceeds the array is rejected with SPMM_ERR_UNSUPPORTED before anything is
+ * launched.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and should come before any stream capture on that
+ * device.  Every call reuses the same array and leaves its contents behind:
+ * calls whose work can overlap on the GPU (other streams, other threads)
+ * race; order them.  Asynchronous on `stream`; results are bitwise
+ * reproducible for given inputs.
+ */
+SPMM_API spmm_status spmm_csr_f32_noalloc(int32_t M, int32_t K, int32_t N, int64_t nnz,
+                                          const int32_t* rowptr, const int32_t* colind,
+                                          const float* vals, const float* B, float* C, void* stream);
+
+/*
  * Optional timing hook.  When `event` (a cudaEvent_t passed as void*) is not
  * NULL, every later exec with this plan records it on the exec stream right
  * after the main SpMM kernel, before the balanced family's fixup kernel, so
