@@ -17,10 +17,10 @@ static int pow2_at_least(int x) {
   return p;
 }
 
-Shape choose_shape(int32_t N, bool bf16, bool vector_ok) {
+Shape choose_shape(int32_t N, bool bf16, bool vector_ok, int chunks_f32) {
   if (vector_ok) {
     const int vec = bf16 ? 8 : 4;
-    const int chunks = bf16 ? SPMM_BF16_CHUNKS : SPMM_LANE_CHUNKS;
+    const int chunks = bf16 ? (chunks_f32 / 2 > 0 ? chunks_f32 / 2 : 1) : chunks_f32;
     const int L = N / vec;  // 16-byte vectors per row (N is a multiple of vec here)
     if (L <= chunks) return Shape{vec, 1, pow2_at_least(L)};
     // G lanes of `chunks` vectors each; rows wider than 32 lanes run as column tiles
@@ -60,7 +60,8 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
   if (!guard.ok) return SPMM_ERR_CUDA;
 
   const bool vector_ok = plan->N % (bf16 ? 8 : 4) == 0 && aligned16(B) && aligned16(C);
-  const Shape s = choose_shape(plan->N, bf16, vector_ok);
+  const Shape s = plan->kernel == SPMM_KERNEL_ROW ? choose_shape(plan->N, bf16, vector_ok)
+                                                  : choose_shape_balanced(plan->N, bf16, vector_ok);
   Launch L{};
   L.M = plan->M;
   L.N = plan->N;

@@ -1,4 +1,4 @@
-// nnz-balanced (merge-path) SpMM kernel and its deterministic fixup.
+// nnz-balanced (merge-path) SpMM kernel.
 //
 // Work items.  The row ends of A (M items) and its nonzeros (nnz items) are
 // merged into one sequence: row i's nonzeros rowptr[i]..rowptr[i+1]-1, then
@@ -12,29 +12,30 @@
 // computes these coordinates once per CTA by binary search over rowptr.
 //
 // One CTA per range [(i0, p0), (i1, p1)) of T items:
-//  1. stages the range's colind and vals in shared memory with 1-D bulk
-//     copies (the TMA engine; the ESIMD kernel's chunked colind/vals loads and
-//     prefetch, Figs. 8-10 of the Intel Max page, and the coalesced row caching
-//     the Sgap page cites from Ge-SpMM), plain loads covering unaligned ends;
-//  2. meanwhile reads rowptr[i0..i1+1] once: marks where each row's
-//     nonzeros start, lists the empty rows whose end lies in the range, and a
-//     block max-scan turns the marks into a row id per staged nonzero; the
-//     empty rows' C rows are stored as zeros, coalesced;
-//  3. splits its nonzeros evenly among W worker groups of G lanes; each
-//     worker streams its nonzeros in batches of U (gathers of B rows issued
-//     before the FMAs that use them; short batches zero-extended), and when
-//     the row id changes stores the finished C row (streaming store) -- or
-//     parks it as a partial in shared memory when the row started before the
-//     worker's nonzeros (slot 0) or continues after them (slot 1);
-//  4. after a barrier, the partials of each row are summed in worker order
-//     (the segmented reduction keyed by row of the Sgap page, done through
-//     shared memory without atomics) and stored to C when the row lies inside
-//     the CTA, else written to the CTA's carry slot 0 (row began before the
-//     range) or 1 (row began inside and continues after it).
+//  1. stages the range's colind and vals and rowptr[i0..i1] in shared memory
+//     with 1-D bulk copies (the TMA engine; the ESIMD kernel's chunked
+//     colind/vals loads and prefetch, Figs. 8-10 of the Intel Max page, and the
+//     coalesced row caching the Sgap page cites from Ge-SpMM), plain loads for
+//     the unaligned ends;
+//  2. cuts the range again into one sub-range per warp with the same search
+//     in shared memory.  A warp is one worker: its 32 lanes form S = 32/G
+//     groups of G lanes, each lane owning NCH 16-byte chunks of the output
+//     row; a step gives S consecutive nonzeros to the S groups (Sgap's
+//     {<1 nnz, c col>, r = S} point), so every branch is uniform in the warp;
+//  3. per batch, issues the gathers of U steps, then accumulates with packed
+//     FMAs.  Where a row ends inside a step, each group only adds the nonzeros
+//     on its side of the end (value 0 otherwise: zero extension), and the S
+//     groups' partial rows are combined by a shuffle butterfly in a fixed
+//     order -- the warp-shuffle segmented reduction keyed by row -- before
+//     group 0 stores the finished C row with a streaming store.  Rows the warp
+//     entered mid-way (head) or that lie across the whole warp (middle) are
+//     parked in shared memory; the row it leaves unfinished stays in registers;
+//  4. after a barrier, each row's pieces are summed in warp order: rows that
+//     lie inside the CTA go to C, the CTA's first and last rows to its carry
+//     slots 0 and 1, which the fixup kernel adds across CTAs in CTA order.
 //
-// The fixup kernel then adds, for every row whose nonzeros cross CTAs, its
-// carry slots in CTA order and writes the C row.  No floating-point atomics
-// anywhere, so C is bitwise reproducible for a given plan.
+// No floating-point atomics anywhere, so C is bitwise reproducible for a given
+// plan.
 #pragma once
 
 #include <climits>
@@ -43,92 +44,85 @@
 #include "spmm_internal.h"
 
 #ifndef SPMM_BAL_LOADS
-#define SPMM_BAL_LOADS 4  // 16-byte B loads in flight per lane (U nonzeros x NCH chunks)
+#define SPMM_BAL_LOADS 8  // 16-byte B loads in flight per lane (U steps x NCH chunks)
 #endif
 #ifndef SPMM_BAL_MIN_BLOCKS
-#define SPMM_BAL_MIN_BLOCKS 1
+#define SPMM_BAL_MIN_BLOCKS 4  // resident CTAs asked of the compiler (fp32, one chunk per lane)
 #endif
 
 namespace spmm {
 
-// Kinds of a worker's parked partial row (its shared-memory slot).
-constexpr int kSlotHead = 1;    // the row began before the worker and ends in it
-constexpr int kSlotMiddle = 2;  // the worker lies entirely inside the row
+// Kinds of a warp's parked partial row (its shared-memory slot).
+constexpr int kSlotHead = 1;    // the row began before the warp and ends in it
+constexpr int kSlotMiddle = 2;  // the warp lies entirely inside the row
 
 template <int NCH>
-struct BalancedUnroll {
+struct BalancedSteps {
   static constexpr int value = SPMM_BAL_LOADS / NCH > 0 ? SPMM_BAL_LOADS / NCH : 1;
 };
 
+// The 64-register budget of 4 resident CTAs fits the fp32 one-chunk shapes
+// without spills; wider or bf16 lanes keep the compiler's own choice.
+template <typename BT, int NCH>
+struct BalancedMinBlocks {
+  static constexpr int value = (sizeof(BT) == 4 && NCH == 1) ? SPMM_BAL_MIN_BLOCKS : 1;
+};
+
 __host__ __device__ constexpr size_t balanced_smem_layout_bytes(int W, int TW, int T) {
-  return size_t(4) * (T + 8) * 4   // colind, vals, row ids, empty-row list
-         + size_t(1) * W * TW * 4  // one parked partial row per worker
+  return size_t(3) * (T + 8) * 4   // colind, vals, rowptr slices
+         + size_t(1) * W * TW * 4  // one parked partial row per warp
          + size_t(1) * W * 8       // slot metadata (local row, kind)
-         + 64 * 4                  // scan scratch, counters, flags
          + 16;                     // mbarrier
 }
 
 template <typename BT, int VEC, int G, int NCH>
-__global__ void __launch_bounds__(kThreads, SPMM_BAL_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
     spmm_balanced_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr,
                          const int32_t* __restrict__ colind, const float* __restrict__ vals,
                          const BT* __restrict__ B, float* __restrict__ C,
                          const int2* __restrict__ part, int32_t T, float* __restrict__ carry,
                          int* __restrict__ err) {
-  constexpr int W = kThreads / G;
-  constexpr int TW = G * VEC * NCH;
-  constexpr int U = BalancedUnroll<NCH>::value;
+  constexpr int S = 32 / G;                // nonzeros per warp step
+  constexpr int W = kThreads / 32;         // warps (workers) per CTA
+  constexpr int TW = G * VEC * NCH;        // columns per tile
+  constexpr int U = BalancedSteps<NCH>::value;  // steps per batch
 
   extern __shared__ __align__(16) unsigned char smem[];
   const int Tpad = T + 8;
   int* s_col = reinterpret_cast<int*>(smem);
   float* s_val = reinterpret_cast<float*>(s_col + Tpad);
-  int* s_row = s_col + 2 * Tpad;    // local row id of each staged nonzero
-  int* s_empty = s_col + 3 * Tpad;  // local ids of empty rows ending in this range
-  float* s_slot = reinterpret_cast<float*>(s_col + 4 * Tpad);  // [W][TW] parked partial rows
+  int* s_rp = s_col + 2 * Tpad;
+  float* s_slot = reinterpret_cast<float*>(s_col + 3 * Tpad);  // [W][TW]
   int2* s_meta = reinterpret_cast<int2*>(s_slot + W * TW);     // [W] (local row, kind)
-  int* s_misc = reinterpret_cast<int*>(s_meta + W);            // [0..7] scan, [8] #empty, [9..10] flags
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_misc + 64);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_meta + W);
 
   const int tid = threadIdx.x;
-  const int warp = tid >> 5, wl = tid & 31;
   const int cta = blockIdx.x;
-  const uint64_t stream_pol = policy_evict_first();
   const int2 beg = __ldg(part + cta);
   const int2 fin = __ldg(part + cta + 1);
   const int i0 = beg.x, p0 = beg.y, i1 = fin.x, p1 = fin.y;
-  const int nbase = p0 & ~3;  // s_col[k], s_val[k], s_row[k] describe nonzero nbase + k
-  const int nnz_here = p1 - p0;
-  const int col0 = blockIdx.y * TW;
+  const int nbase = p0 & ~3;  // s_col[k], s_val[k] hold nonzero nbase + k
+  const int rbase = i0 & ~3;  // s_rp[k] holds rowptr[rbase + k]; rows i0..i1 are staged
+  const uint64_t stream_pol = policy_evict_first();
 
-  // ---- 1. launch the bulk copies; init row ids ------------------------------
+  // ---- 1. stage the range -------------------------------------------------
   const uint32_t bar = smem_addr(s_bar);
-  const bool bulk_ok = ((reinterpret_cast<uintptr_t>(colind) | reinterpret_cast<uintptr_t>(vals)) & 15) == 0;
-  const int ca = (p0 + 3) & ~3, cb = p1 & ~3;  // 16-byte aligned interior of [p0, p1)
+  const bool bulk_ok = ((reinterpret_cast<uintptr_t>(colind) | reinterpret_cast<uintptr_t>(vals) |
+                         reinterpret_cast<uintptr_t>(rowptr)) & 15) == 0;
+  const int ca = (p0 + 3) & ~3, cb = p1 & ~3;        // 16-byte aligned interior of [p0, p1)
+  const int ra = (i0 + 3) & ~3, rb = (i1 + 1) & ~3;  // ... of [i0, i1 + 1)
   const bool c_bulk = bulk_ok && cb > ca;
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    s_misc[8] = 0;
-  }
-  for (int k = p0 - nbase + tid; k < p1 - nbase; k += kThreads) s_row[k] = -1;
+  const bool r_bulk = bulk_ok && rb > ra;
+  if (tid == 0) mbar_init(bar, 1);
   for (int k = tid; k < W; k += kThreads) s_meta[k] = make_int2(-1, 0);
   __syncthreads();
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar, c_bulk ? 8u * uint32_t(cb - ca) : 0u);
+    mbar_arrive_expect_tx(bar, (c_bulk ? 8u * uint32_t(cb - ca) : 0u) + (r_bulk ? 4u * uint32_t(rb - ra) : 0u));
     if (c_bulk) {
       bulk_g2s(smem_addr(s_col + (ca - nbase)), colind + ca, 4u * uint32_t(cb - ca), bar);
       bulk_g2s(smem_addr(s_val + (ca - nbase)), vals + ca, 4u * uint32_t(cb - ca), bar);
     }
-    // Does the first nonzero belong to a row that began before the range, and
-    // does the last nonzero's row continue after it?
-    const int rs0 = ld_stream(rowptr + i0, stream_pol);
-    const int re0 = i0 < M ? ld_stream(rowptr + i0 + 1, stream_pol) : rs0;
-    const bool first_before = nnz_here > 0 && rs0 < p0 && p0 < re0;
-    if (first_before) s_row[p0 - nbase] = 0;
-    s_misc[9] = first_before;
-    const int rs1 = ld_stream(rowptr + i1, stream_pol);
-    const int re1 = i1 < M ? ld_stream(rowptr + i1 + 1, stream_pol) : rs1;
-    s_misc[10] = nnz_here > 0 && rs1 < p1 && re1 > p1;
+    if (r_bulk) bulk_g2s(smem_addr(s_rp + (ra - rbase)), rowptr + ra, 4u * uint32_t(rb - ra), bar);
   }
   if (c_bulk) {  // at most 3 leading and 3 trailing nonzeros
     const int g = tid < 4 ? p0 + tid : cb + (tid - 4);
@@ -142,54 +136,11 @@ __global__ void __launch_bounds__(kThreads, SPMM_BAL_MIN_BLOCKS)
       s_val[g - nbase] = ld_stream(vals + g, stream_pol);
     }
   }
-  // ---- 2. row starts and empty rows -----------------------------------------
-  for (int r = i0 + tid; r <= i1 && r < M; r += kThreads) {
-    const int rs = ld_stream(rowptr + r, stream_pol);
-    const int re = ld_stream(rowptr + r + 1, stream_pol);
-    if (rs < re) {
-      if (rs >= p0 && rs < p1) s_row[rs - nbase] = r - i0;
-    } else if (r < i1) {
-      s_empty[atomicAdd(s_misc + 8, 1)] = r;
-    }
-  }
-  __syncthreads();
-  {  // zero the empty rows' C tiles: consecutive threads store consecutive 16-byte pieces
-    constexpr int kPieces = TW / (VEC >= 4 ? 4 : 1);
-    const int n_empty = s_misc[8];
-    for (int u = tid; u < n_empty * kPieces; u += kThreads) {
-      const int e = u / kPieces;
-      const int col = col0 + (u - e * kPieces) * (VEC >= 4 ? 4 : 1);
-      if (col < N) {
-        float* dst = C + size_t(s_empty[e]) * N + col;
-        if constexpr (VEC >= 4) {
-          st_stream4(dst, 0.f, 0.f, 0.f, 0.f);
-        } else {
-          st_stream1(dst, 0.f);
-        }
-      }
-    }
-  }
-  {  // inclusive max-scan of the row-start marks -> row id of every nonzero
-    const int per_t = (nnz_here + kThreads - 1) / kThreads;
-    const int a = p0 - nbase + tid * per_t;
-    const int b = min(a + per_t, p1 - nbase);
-    int run = -1;
-    for (int k = a; k < b; ++k) run = max(run, s_row[k]);
-    int incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (wl >= o) incl = max(incl, y);
-    }
-    if (wl == 31) s_misc[warp] = incl;
-    __syncthreads();
-    int prefix = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (wl == 0) prefix = -1;
-    for (int x = 0; x < warp; ++x) prefix = max(prefix, s_misc[x]);
-    for (int k = a; k < b; ++k) {
-      prefix = max(prefix, s_row[k]);
-      s_row[k] = prefix;
-    }
+  if (r_bulk) {
+    const int g = tid < 4 ? i0 + tid : rb + (tid - 4);
+    if (tid < 8 && ((tid < 4 && g < ra) || (tid >= 4 && g <= i1))) s_rp[g - rbase] = ld_stream(rowptr + g, stream_pol);
+  } else {
+    for (int g = i0 + tid; g <= i1; g += kThreads) s_rp[g - rbase] = ld_stream(rowptr + g, stream_pol);
   }
   const bool staged = mbar_wait_bounded(bar, 0, kSpinLimit);
   if (__syncthreads_or(!staged)) {
@@ -198,153 +149,186 @@ __global__ void __launch_bounds__(kThreads, SPMM_BAL_MIN_BLOCKS)
     return;
   }
 
-  // ---- 3. stream this worker's nonzeros -------------------------------------
-  const int w = tid / G;
-  const int lane = tid & (G - 1);
-  const int per_w = (nnz_here + W - 1) / W;
-  const int q0 = p0 + min(w * per_w, nnz_here);
-  const int q1 = p0 + min((w + 1) * per_w, nnz_here);
-  int coff[NCH], coffl[NCH];  // store offsets; load offsets clamped into the row
-  bool cok[NCH];
+  // ---- 2. this warp's sub-range ---------------------------------------------
+  const int w = tid >> 5;
+  const int lane = tid & 31;
+  const int grp = lane / G;       // which nonzero of a step this lane's group takes
+  const int gl = lane & (G - 1);  // lane within its group
+  const int* rp = s_rp + (i0 - rbase);  // rp[r] = rowptr[i0 + r], 0 <= r <= i1 - i0
+  const int items = (i1 - i0) + (p1 - p0);
+  const int Tw = T / W;
+  auto find_row = [&](int dl) {  // first local row whose end lies at or after diagonal dl
+    int lo = 0, hi = i1 - i0;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (rp[mid + 1] - p0 + mid >= dl) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+  };
+  const int dl0 = min(w * Tw, items);
+  const int dl1 = min(dl0 + Tw, items);
+  const int rw0 = find_row(dl0), rw1 = find_row(dl1);
+  const int pw0 = p0 + dl0 - rw0, pw1 = p0 + dl1 - rw1;
+
+  const int col0 = blockIdx.y * TW;
+  int coff[NCH];
+  const BT* bl[NCH];  // this lane's slice of B row 0 (clamped into the row); row c is bl[ch] + c*N
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
-    coff[ch] = col0 + (ch * G + lane) * VEC;
-    coffl[ch] = min(coff[ch], N - VEC);
-    cok[ch] = coff[ch] < N;
+    coff[ch] = col0 + (ch * G + gl) * VEC;
+    bl[ch] = B + min(coff[ch], N - VEC);
   }
-  auto slot_ptr = [&](int worker, int ch) { return s_slot + worker * TW + (ch * G + lane) * VEC; };
-  // The worker's unfinished last row, when the row also began in this worker:
-  // kept in registers across the barrier and completed by this worker.
-  bool has_tail = false;
-  int tail_row = -1;
-  float acc[NCH][VEC];
+  const int* colw = s_col - nbase + grp;  // colw[a] = colind of nonzero a + grp (staged)
+  const float* valw = s_val - nbase + grp;
+  auto slot_ptr = [&](int worker, int ch) { return s_slot + worker * TW + (ch * G + gl) * VEC; };
+  FVec<VEC> acc[NCH];
 #pragma unroll
-  for (int ch = 0; ch < NCH; ++ch)
+  for (int ch = 0; ch < NCH; ++ch) acc[ch].zero();
+  // Combine the S groups' partial rows: afterwards every group holds the sum.
+  auto butterfly = [&] {
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) acc[ch][j] = 0.f;
-
-  if (q0 < q1) {
-    const int first = s_row[q0 - nbase];
-    const bool head_partial = q0 > p0 ? s_row[q0 - 1 - nbase] == first : s_misc[9] != 0;
-    // Finished row `r`: C row, or a parked head partial when it began before q0.
-    auto flush = [&](int r) {
-      if (r == first && head_partial) {
+    for (int o = G; o < 32; o <<= 1)
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) store_f4<VEC>(slot_ptr(w, ch), acc[ch]);
-        if (lane == 0) s_meta[w] = make_int2(r, kSlotHead);
-      } else {
-        float* crow = C + size_t(i0 + r) * N;
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch)
-          if (cok[ch]) store_c<VEC>(crow + coff[ch], acc[ch]);
-      }
+      for (int ch = 0; ch < NCH; ++ch) acc[ch].add_shfl_xor(o);
+  };
+  auto store_row = [&](float* dst) {  // group 0 writes the row slice (streaming)
+    if (grp == 0) {
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch)
+        if (coff[ch] < N) store_c<VEC>(dst + coff[ch], acc[ch]);
+    }
+  };
+  auto park = [&](int r, int kind) {
+    if (grp == 0) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) acc[ch][j] = 0.f;
-    };
+      for (int ch = 0; ch < NCH; ++ch) acc[ch].store_plain(slot_ptr(w, ch));
+    }
+    if (lane == 0) s_meta[w] = make_int2(r, kind);
+  };
 
-    int cur = first;
-    for (int q = q0; q < q1; q += U) {
-      // Issue the batch's gathers first (a padded slot re-reads the worker's
-      // last row); values and row ids are re-read from shared memory
-      // afterwards, so only the B slices occupy registers while loads fly.
-      BSlice<BT, VEC> bs[U][NCH];
+  // ---- 3. stream the sub-range --------------------------------------------
+  int r = rw0;
+  bool began_before = rp[r] < pw0;
+  int next_end = r < rw1 ? rp[r + 1] : INT_MAX;
+  float* const crow0 = C + size_t(i0) * N;
+  // Row r ends: finish it (all warp-uniform).
+  auto end_row = [&] {
+    if (rp[r] != rp[r + 1]) {  // an empty row's accumulators are still zero
+      butterfly();
+      if (began_before) park(r, kSlotHead); else store_row(crow0 + size_t(r) * N);
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const BT* brow = B + size_t(s_col[min(q + u, q1 - 1) - nbase]) * N;
+      for (int ch = 0; ch < NCH; ++ch) acc[ch].zero();
+    } else {
+      store_row(crow0 + size_t(r) * N);
+    }
+    ++r;
+    began_before = false;
+    next_end = r < rw1 ? rp[r + 1] : INT_MAX;
+  };
+  // One step: the S groups take nonzeros a .. a+S-1 (group grp: n = a + grp,
+  // value v, B slice b); rows ending inside the step are completed in order.
+  auto step = [&](int a, float v, const BSlice<BT, VEC> (&bs)[NCH]) {
+    FVec<VEC> b[NCH];
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(brow + coffl[ch]);
-      }
+    for (int ch = 0; ch < NCH; ++ch) bs[ch].widen(b[ch]);
+    const int n = a + grp;
+    int lo = a;
+    while (next_end <= a + S) {  // a row ends inside (or right after) this step
+      const float2 vv = pair((n >= lo && n < next_end) ? v : 0.f);
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int k = min(q + u, q1 - 1) - nbase;
-        const int r = s_row[k];  // a padded slot repeats the last row: no flush
-        const float v = q + u < q1 ? s_val[k] : 0.f;
-        if (r != cur) {
-          flush(cur);
-          cur = r;
-        }
-        const uint64_t vv = pack_pair(v);
+      for (int ch = 0; ch < NCH; ++ch) acc[ch].fma(vv, b[ch]);
+      lo = next_end;
+      end_row();
+    }
+    const float2 vv = pair(n >= lo ? v : 0.f);
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) acc[ch].fma(vv, b[ch]);
+  };
+  int q = pw0;
+  for (; q + U * S <= pw1; q += U * S) {  // full batches
+    BSlice<BT, VEC> bs[U][NCH];
+#pragma unroll
+    for (int s = 0; s < U; ++s) {  // gathers first
+      const size_t roff = size_t(colw[q + s * S]) * N;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
+    }
+    if (next_end > q + U * S) {  // no row ends inside the batch
+#pragma unroll
+      for (int s = 0; s < U; ++s) {
+        const float2 vv = pair(valw[q + s * S]);
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
-          float b[VEC];
-          bs[u][ch].widen(b);
-          axpy<VEC>(acc[ch], v, vv, b);
+          FVec<VEC> b;
+          bs[s][ch].widen(b);
+          acc[ch].fma(vv, b);
         }
       }
-    }
-    const bool tail_partial = q1 < p1 ? s_row[q1 - nbase] == cur : s_misc[10] != 0;
-    if (!tail_partial) {
-      flush(cur);
-    } else if (cur == first && head_partial) {  // the worker lies inside one row
+    } else {
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) store_f4<VEC>(slot_ptr(w, ch), acc[ch]);
-      if (lane == 0) s_meta[w] = make_int2(cur, kSlotMiddle);
-    } else {  // row `cur` began here and continues after this worker
-      has_tail = true;
-      tail_row = cur;
+      for (int s = 0; s < U; ++s) step(q + s * S, valw[q + s * S], bs[s]);
     }
+  }
+  if (q < pw1) {  // short last batch: slots past the sub-range re-read its last nonzero's row, value 0
+    BSlice<BT, VEC> bs[U][NCH];
+#pragma unroll
+    for (int s = 0; s < U; ++s) {
+      const size_t roff = size_t(colw[min(q + s * S, pw1 - 1 - grp)]) * N;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
+    }
+#pragma unroll
+    for (int s = 0; s < U; ++s) {
+      const int a = q + s * S;
+      if (a >= pw1) break;
+      step(a, a + grp < pw1 ? valw[a] : 0.f, bs[s]);
+    }
+  }
+  while (r < rw1) end_row();  // rows ending exactly at the sub-range end (empty rows too)
+  bool has_tail = false;
+  const int tail_row = r;
+  if (i0 + r < M && rp[r] < pw1) {  // row r continues after this warp
+    butterfly();
+    if (began_before) park(r, kSlotMiddle); else has_tail = true;
   }
   __syncthreads();
 
-  // ---- 4. complete rows split between workers -------------------------------
-  // A chain is a row's partials in worker order: a start (worker 0's parked
-  // partial of the CTA's first row, or a worker's register tail), then parked
-  // middles, then possibly a parked head where the row ends.
-  auto walk = [&](int row, int from) {  // add the parked pieces of `row` from worker `from` on
+  // ---- 4. complete rows split between warps ---------------------------------
+  auto walk = [&](int row, int from) {  // add the parked pieces of `row` from warp `from` on
     for (int w2 = from; w2 < W; ++w2) {
       const int2 m = s_meta[w2];
       if (m.x != row) return false;  // the row continues past this CTA's nonzeros
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) {
-        float piece[VEC];
-        load_f4<VEC>(slot_ptr(w2, ch), piece);
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) acc[ch][j] += piece[j];
+        FVec<VEC> piece;
+        piece.load_plain(slot_ptr(w2, ch));
+        acc[ch].add(piece);
       }
       if (m.y == kSlotHead) return true;
     }
     return false;
   };
   if (w == 0 && s_meta[0].x >= 0) {  // the CTA's first row began before the CTA
-    const int2 m0 = s_meta[0];
-    float keep[NCH][VEC];  // worker 0 may also hold a register tail
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        keep[ch][j] = acc[ch][j];
-        acc[ch][j] = 0.f;
-      }
-    walk(m0.x, 0);
-    float* dst = carry + size_t(cta) * 2 * N;  // slot 0: completed by the fixup
+    FVec<VEC> keep[NCH];             // warp 0 may also hold a register tail
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
-      if (cok[ch]) store_f4<VEC>(dst + coff[ch], acc[ch]);
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) acc[ch][j] = keep[ch][j];
+      keep[ch] = acc[ch];
+      acc[ch].zero();
     }
+    walk(s_meta[0].x, 0);
+    store_row(carry + size_t(cta) * 2 * N);  // slot 0: completed by the fixup
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) acc[ch] = keep[ch];
   }
   if (has_tail) {
-    const bool covers_end = walk(tail_row, w + 1);
-    if (covers_end) {
-      float* crow = C + size_t(i0 + tail_row) * N;
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch)
-        if (cok[ch]) store_c<VEC>(crow + coff[ch], acc[ch]);
-    } else {
-      float* dst = carry + (size_t(cta) * 2 + 1) * N;  // slot 1: row continues after the CTA
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch)
-        if (cok[ch]) store_f4<VEC>(dst + coff[ch], acc[ch]);
-    }
+    if (walk(tail_row, w + 1)) store_row(crow0 + size_t(tail_row) * N);
+    else store_row(carry + (size_t(cta) * 2 + 1) * N);  // slot 1: row continues after the CTA
   }
 }
 
 template <typename BT, int VEC, int G, int NCH>
 cudaError_t launch_balanced_t(const Launch& L) {
-  constexpr int W = kThreads / G;
+  constexpr int W = kThreads / 32;
   constexpr int TW = G * VEC * NCH;
   const size_t smem = balanced_smem_layout_bytes(W, TW, L.items_per_cta);
   static bool attr_set[kMaxDevices] = {};  // per instantiation and device

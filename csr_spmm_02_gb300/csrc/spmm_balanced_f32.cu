@@ -6,7 +6,7 @@ namespace spmm {
 cudaError_t launch_balanced_f32(const Launch& L, Shape s) {
 #define X(V, GG, NC) \
   if (s.vec == V && s.G == GG && s.nch == NC) return launch_balanced_t<float, V, GG, NC>(L);
-  SPMM_VECTOR_SHAPES(X, 4, SPMM_LANE_CHUNKS)
+  SPMM_VECTOR_SHAPES(X, 4, SPMM_BAL_CHUNKS)
   SPMM_SCALAR_SHAPES(X)
 #undef X
   return cudaErrorInvalidConfiguration;

@@ -1,10 +1,11 @@
 // Device building blocks shared by the SpMM kernels (sm_103a).
 //
+//  * FVec<VEC>: a lane's VEC fp32 accumulators, as float2 pairs for packed
+//    FMAs (fma.rn.f32x2: two IEEE fp32 FMAs per instruction, bitwise equal
+//    to two scalar fmaf).
 //  * BSlice<BT, VEC>: one lane's VEC consecutive elements of a B row, loaded
 //    raw in one 16-byte (or scalar) load and widened to fp32 at use.  bf16 is
 //    the top half of an IEEE binary32, so widening is an exact 16-bit shift.
-//  * axpy: acc += v * b with packed fma.rn.f32x2 (two IEEE fp32 FMAs per
-//    instruction; bitwise equal to two scalar fmaf).
 //  * streaming (evict-first) stores of C rows, which are written once.
 //  * 1-D bulk copies (cp.async.bulk, the TMA engine's non-tensor form) into
 //    shared memory completed on an mbarrier, with a bounded wait.
@@ -56,7 +57,63 @@ __device__ __forceinline__ float ld_stream(const float* p, uint64_t pol) {
 }
 
 // ---------------------------------------------------------------------------
-// B slices
+// FVec<VEC>: VEC fp32 values of one lane.  Even widths are kept as float2
+// pairs so packed FMAs (fma.rn.f32x2 through __ffma2_rn: two IEEE fp32 FMAs,
+// bitwise equal to two fmaf) need no register moves.
+// ---------------------------------------------------------------------------
+template <int VEC>
+struct FVec {
+  static_assert(VEC % 2 == 0, "even widths only");
+  float2 p[VEC / 2];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) p[j] = make_float2(0.f, 0.f);
+  }
+  __device__ __forceinline__ void fma(float2 vv, const FVec& b) {  // this += (v, v) * b
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) p[j] = __ffma2_rn(vv, b.p[j], p[j]);
+  }
+  __device__ __forceinline__ void add(const FVec& o) {
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) p[j] = make_float2(p[j].x + o.p[j].x, p[j].y + o.p[j].y);
+  }
+  __device__ __forceinline__ void add_shfl_xor(int mask) {
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) {
+      p[j].x += __shfl_xor_sync(0xffffffffu, p[j].x, mask);
+      p[j].y += __shfl_xor_sync(0xffffffffu, p[j].y, mask);
+    }
+  }
+  __device__ __forceinline__ void load_plain(const float* src) {  // 16-byte aligned
+#pragma unroll
+    for (int j = 0; j < VEC / 2; j += 2) {
+      const float4 t = *reinterpret_cast<const float4*>(src + 2 * j);
+      p[j] = make_float2(t.x, t.y);
+      p[j + 1] = make_float2(t.z, t.w);
+    }
+  }
+  __device__ __forceinline__ void store_plain(float* dst) const {
+#pragma unroll
+    for (int j = 0; j < VEC / 2; j += 2)
+      *reinterpret_cast<float4*>(dst + 2 * j) = make_float4(p[j].x, p[j].y, p[j + 1].x, p[j + 1].y);
+  }
+};
+
+template <>
+struct FVec<1> {
+  float x;
+  __device__ __forceinline__ void zero() { x = 0.f; }
+  __device__ __forceinline__ void fma(float2 vv, const FVec& b) { x = fmaf(vv.x, b.x, x); }
+  __device__ __forceinline__ void add(const FVec& o) { x += o.x; }
+  __device__ __forceinline__ void add_shfl_xor(int mask) { x += __shfl_xor_sync(0xffffffffu, x, mask); }
+  __device__ __forceinline__ void load_plain(const float* src) { x = *src; }
+  __device__ __forceinline__ void store_plain(float* dst) const { *dst = x; }
+};
+
+// ---------------------------------------------------------------------------
+// B slices: one 16-byte (or scalar) load of a lane's VEC elements of a B row,
+// widened to fp32 at use.  bf16 is the top half of an IEEE binary32, so
+// widening is an exact 16-bit shift.
 // ---------------------------------------------------------------------------
 template <typename BT, int VEC>
 struct BSlice;
@@ -65,18 +122,9 @@ template <>
 struct BSlice<float, 4> {
   float4 r;
   __device__ __forceinline__ void load(const float* p) { r = __ldg(reinterpret_cast<const float4*>(p)); }
-  __device__ __forceinline__ void load_if(const float* p, bool pred) {
-#if SPMM_B_EVICT_LAST
-    r = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (pred)
-      asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
-                   : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "l"(p), "l"(policy_evict_last()));
-#else
-    r = pred ? __ldg(reinterpret_cast<const float4*>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
-#endif
-  }
-  __device__ __forceinline__ void widen(float (&o)[4]) const {
-    o[0] = r.x; o[1] = r.y; o[2] = r.z; o[3] = r.w;
+  __device__ __forceinline__ void widen(FVec<4>& o) const {
+    o.p[0] = make_float2(r.x, r.y);
+    o.p[1] = make_float2(r.z, r.w);
   }
 };
 
@@ -84,77 +132,33 @@ template <>
 struct BSlice<float, 1> {
   float r;
   __device__ __forceinline__ void load(const float* p) { r = __ldg(p); }
-  __device__ __forceinline__ void load_if(const float* p, bool pred) { r = pred ? __ldg(p) : 0.f; }
-  __device__ __forceinline__ void widen(float (&o)[1]) const { o[0] = r; }
+  __device__ __forceinline__ void widen(FVec<1>& o) const { o.x = r; }
 };
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float2 bf16x2_widen(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
 
 template <>
 struct BSlice<uint16_t, 8> {
   uint4 r;
   __device__ __forceinline__ void load(const uint16_t* p) { r = __ldg(reinterpret_cast<const uint4*>(p)); }
-  __device__ __forceinline__ void load_if(const uint16_t* p, bool pred) {
-#if SPMM_B_EVICT_LAST
-    r = make_uint4(0u, 0u, 0u, 0u);
-    if (pred)
-      asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-                   : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p), "l"(policy_evict_last()));
-#else
-    r = pred ? __ldg(reinterpret_cast<const uint4*>(p)) : make_uint4(0u, 0u, 0u, 0u);
-#endif
-  }
-  __device__ __forceinline__ void widen(float (&o)[8]) const {
-    o[0] = bf16_lo(r.x); o[1] = bf16_hi(r.x);
-    o[2] = bf16_lo(r.y); o[3] = bf16_hi(r.y);
-    o[4] = bf16_lo(r.z); o[5] = bf16_hi(r.z);
-    o[6] = bf16_lo(r.w); o[7] = bf16_hi(r.w);
+  __device__ __forceinline__ void widen(FVec<8>& o) const {
+    o.p[0] = bf16x2_widen(r.x);
+    o.p[1] = bf16x2_widen(r.y);
+    o.p[2] = bf16x2_widen(r.z);
+    o.p[3] = bf16x2_widen(r.w);
   }
 };
 
 template <>
 struct BSlice<uint16_t, 1> {
   unsigned short r;
-  __device__ __forceinline__ void load(const uint16_t* p) {
-    r = __ldg(reinterpret_cast<const unsigned short*>(p));
-  }
-  __device__ __forceinline__ void load_if(const uint16_t* p, bool pred) {
-    r = pred ? __ldg(reinterpret_cast<const unsigned short*>(p)) : (unsigned short)0;
-  }
-  __device__ __forceinline__ void widen(float (&o)[1]) const { o[0] = __uint_as_float(uint32_t(r) << 16); }
+  __device__ __forceinline__ void load(const uint16_t* p) { r = __ldg(reinterpret_cast<const unsigned short*>(p)); }
+  __device__ __forceinline__ void widen(FVec<1>& o) const { o.x = __uint_as_float(uint32_t(r) << 16); }
 };
 
-// ---------------------------------------------------------------------------
-// acc += v * b.  The scalar v is packed once per nonzero into a (v, v) pair
-// that every packed FMA of that nonzero reuses.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t pack_pair(float v) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
-  return r;
-}
-
-__device__ __forceinline__ void fma2(float& a0, float& a1, uint64_t vv, float b0, float b1) {
-  asm("{\n\t.reg .b64 rb, rc;\n\t"
-      "mov.b64 rb, {%3, %4};\n\t"
-      "mov.b64 rc, {%0, %1};\n\t"
-      "fma.rn.f32x2 rc, %2, rb, rc;\n\t"
-      "mov.b64 {%0, %1}, rc;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "l"(vv), "f"(b0), "f"(b1));
-}
-
-template <int VEC>
-__device__ __forceinline__ void axpy(float (&acc)[VEC], float v, uint64_t vv, const float (&b)[VEC]) {
-  if constexpr (VEC % 2 == 0) {
-#pragma unroll
-    for (int j = 0; j < VEC; j += 2) fma2(acc[j], acc[j + 1], vv, b[j], b[j + 1]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) acc[j] = fmaf(v, b[j], acc[j]);
-  }
-}
+__device__ __forceinline__ float2 pair(float v) { return make_float2(v, v); }
 
 // ---------------------------------------------------------------------------
 // C stores (each C element is written once: streaming / evict-first)
@@ -177,39 +181,12 @@ __device__ __forceinline__ void st_stream1(float* p, float x) {
 }
 
 template <int VEC>
-__device__ __forceinline__ void store_c(float* p, const float (&a)[VEC]) {
-  if constexpr (VEC % 4 == 0) {
-#pragma unroll
-    for (int j = 0; j < VEC; j += 4) st_stream4(p + j, a[j], a[j + 1], a[j + 2], a[j + 3]);
+__device__ __forceinline__ void store_c(float* p, const FVec<VEC>& a) {
+  if constexpr (VEC == 1) {
+    st_stream1(p, a.x);
   } else {
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) st_stream1(p + j, a[j]);
-  }
-}
-
-template <int VEC>
-__device__ __forceinline__ void store_f4(float* p, const float (&a)[VEC]) {  // plain store
-  if constexpr (VEC % 4 == 0) {
-#pragma unroll
-    for (int j = 0; j < VEC; j += 4)
-      *reinterpret_cast<float4*>(p + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) p[j] = a[j];
-  }
-}
-
-template <int VEC>
-__device__ __forceinline__ void load_f4(const float* p, float (&a)[VEC]) {  // plain load
-  if constexpr (VEC % 4 == 0) {
-#pragma unroll
-    for (int j = 0; j < VEC; j += 4) {
-      float4 t = *reinterpret_cast<const float4*>(p + j);
-      a[j] = t.x; a[j + 1] = t.y; a[j + 2] = t.z; a[j + 3] = t.w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) a[j] = p[j];
+    for (int j = 0; j < VEC / 2; j += 2) st_stream4(p + 2 * j, a.p[j].x, a.p[j].y, a.p[j + 1].x, a.p[j + 1].y);
   }
 }
 

@@ -6,6 +6,27 @@
 
 #include "../../include/spmm.h"
 
+// 16-byte chunks of the output row each lane owns (fp32: 4 columns per chunk;
+// bf16 B: 8 columns per chunk, so half as many chunks).  Wider lane slices
+// spread each nonzero's bookkeeping over fewer lanes.
+#ifndef SPMM_LANE_CHUNKS
+#define SPMM_LANE_CHUNKS 1
+#endif
+#define SPMM_BF16_CHUNKS (SPMM_LANE_CHUNKS / 2 > 0 ? SPMM_LANE_CHUNKS / 2 : 1)
+// The same for the balanced kernel (its warps split into 32/G groups that
+// take consecutive nonzeros, so wider lane slices mean more nonzeros per step).
+#ifndef SPMM_BAL_CHUNKS
+#define SPMM_BAL_CHUNKS 1
+#endif
+#define SPMM_BAL_BF16_CHUNKS (SPMM_BAL_CHUNKS / 2 > 0 ? SPMM_BAL_CHUNKS / 2 : 1)
+
+// (VEC, G, NCH) shapes compiled for each kernel: small rows use one lane with
+// 1, 2 or 4 chunks; wider rows use G lanes with the standard chunk count.
+#define SPMM_VECTOR_SHAPES(X, V, NC)                                                            \
+  X(V, 1, 1) X(V, 1, 2) X(V, 1, 4) X(V, 2, NC) X(V, 4, NC) X(V, 8, NC) X(V, 16, NC) X(V, 32, NC)
+#define SPMM_SCALAR_SHAPES(X) X(1, 8, 1) X(1, 32, 1)
+
+
 struct spmm_plan_s {
   int32_t M = 0;
   int64_t nnz = 0;
@@ -56,7 +77,13 @@ struct Shape {
   int tile_width() const { return G * vec * nch; }
 };
 
-Shape choose_shape(int32_t N, bool bf16, bool vector_ok);
+Shape choose_shape(int32_t N, bool bf16, bool vector_ok, int chunks_f32);
+inline Shape choose_shape(int32_t N, bool bf16, bool vector_ok) {
+  return choose_shape(N, bf16, vector_ok, SPMM_LANE_CHUNKS);
+}
+inline Shape choose_shape_balanced(int32_t N, bool bf16, bool vector_ok) {
+  return choose_shape(N, bf16, vector_ok, SPMM_BAL_CHUNKS);
+}
 
 cudaError_t launch_row_f32(const Launch& L, Shape s);
 cudaError_t launch_row_bf16(const Launch& L, Shape s);
@@ -67,20 +94,6 @@ cudaError_t launch_fixup(const Launch& L);
 cudaError_t launch_partition(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t T, int32_t P, int2* part,
                              cudaStream_t stream);
 
-
-// 16-byte chunks of the output row each lane owns (fp32: 4 columns per chunk;
-// bf16 B: 8 columns per chunk, so half as many chunks).  Wider lane slices
-// spread each nonzero's bookkeeping over fewer lanes.
-#ifndef SPMM_LANE_CHUNKS
-#define SPMM_LANE_CHUNKS 1
-#endif
-#define SPMM_BF16_CHUNKS (SPMM_LANE_CHUNKS / 2 > 0 ? SPMM_LANE_CHUNKS / 2 : 1)
-
-// (VEC, G, NCH) shapes compiled for each kernel: small rows use one lane with
-// 1, 2 or 4 chunks; wider rows use G lanes with the standard chunk count.
-#define SPMM_VECTOR_SHAPES(X, V, NC)                                                            \
-  X(V, 1, 1) X(V, 1, 2) X(V, 1, 4) X(V, 2, NC) X(V, 4, NC) X(V, 8, NC) X(V, 16, NC) X(V, 32, NC)
-#define SPMM_SCALAR_SHAPES(X) X(1, 8, 1) X(1, 32, 1)
 
 constexpr int kDefaultItemsPerCta = 2048;
 constexpr int kMaxItemsPerCta = 8192;

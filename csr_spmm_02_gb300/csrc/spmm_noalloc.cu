@@ -100,7 +100,7 @@ extern "C" SPMM_API spmm_status spmm_csr_f32_noalloc(int32_t M, int32_t K, int32
   L.carry = carry;
   L.err = err;
   L.stream = s;
-  cudaError_t e = launch_balanced_f32(L, choose_shape(N, false, vector_ok));
+  cudaError_t e = launch_balanced_f32(L, choose_shape_balanced(N, false, vector_ok));
   if (e == cudaSuccess) e = launch_fixup(L);
   return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
 }

@@ -65,10 +65,10 @@ __global__ void __launch_bounds__(kThreads) validate_kernel(const int32_t* __res
   if (bad) atomicOr(flag, bad);
 }
 
-// One warp per CTA range c.  If a row's nonzeros start inside range c and run
-// past its end (carry slot 1 of c), add slot 1 of c and slot 0 of every
-// following range up to the one holding the row's last nonzero, in range
-// order, and write the C row.
+// One warp per CTA range c.  If a row starts inside range c and its end item
+// lies in a later range (carry slot 1 of c), add slot 1 of c and slot 0 of
+// every following range up to the one holding the row's end, in range order,
+// and write the C row.
 __global__ void __launch_bounds__(kThreads) spmm_fixup_kernel(int32_t M, int32_t N,
                                                               const int32_t* __restrict__ rowptr,
                                                               const int2* __restrict__ part, int32_t P,
@@ -79,13 +79,12 @@ __global__ void __launch_bounds__(kThreads) spmm_fixup_kernel(int32_t M, int32_t
   if (c >= P) return;
   const int2 beg = __ldg(part + c);
   const int2 fin = __ldg(part + c + 1);
-  const int row = fin.x;  // the only row that can start in range c and continue after it
+  const int row = fin.x;  // the row whose end item is the first one after range c
   if (row >= M) return;
   const int rs = __ldg(rowptr + row);
-  const int re = __ldg(rowptr + row + 1);
-  if (rs < beg.y || rs >= fin.y || re <= fin.y) return;
+  if (rs < beg.y || rs >= fin.y) return;  // the row does not start inside range c
   int last = c + 1;
-  while (__ldg(part + last + 1).y < re) ++last;  // range `last` holds the row's last nonzero
+  while (__ldg(part + last + 1).x == row) ++last;  // range `last` holds the row's end item
   for (int n = lane; n < N; n += 32) {
     float s = carry[(size_t(c) * 2 + 1) * N + n];
     for (int c2 = c + 1; c2 <= last; ++c2) s += carry[(size_t(c2) * 2) * N + n];

@@ -60,17 +60,16 @@ __global__ void __launch_bounds__(kThreads, SPMM_ROW_MIN_BLOCKS)
   // Loads use offsets clamped into the row (a lane past N re-reads a valid
   // slice it never stores), so the inner loop needs no column predicate.
   const int col0 = blockIdx.y * (G * VEC * NCH);
-  int coff[NCH], coffl[NCH];
+  int coff[NCH];
+  const BT* bl[NCH];  // this lane's slice of B row 0; row c is bl[ch] + c*N
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
     coff[ch] = col0 + (ch * G + lane) * VEC;
-    coffl[ch] = min(coff[ch], N - VEC);
+    bl[ch] = B + min(coff[ch], N - VEC);
   }
-  float acc[NCH][VEC];
+  FVec<VEC> acc[NCH];
 #pragma unroll
-  for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) acc[ch][j] = 0.f;
+  for (int ch = 0; ch < NCH; ++ch) acc[ch].zero();
 
   const uint64_t stream_pol = policy_evict_first();
   const int start = ld_stream(rowptr + row, stream_pol);
@@ -82,25 +81,42 @@ __global__ void __launch_bounds__(kThreads, SPMM_ROW_MIN_BLOCKS)
       cv[j] = make_int2(ld_stream(colind + base + j, stream_pol),
                         ld_stream(reinterpret_cast<const int*>(vals) + base + j, stream_pol));
     __syncwarp(gmask);
-    for (int t = 0; t < cnt; t += U) {
-      // Gathers first (a padded slot re-reads the chunk's last row); values
-      // are re-read from shared memory afterwards to keep registers for loads.
+    int t = 0;
+    for (; t + U <= cnt; t += U) {  // full batches: gathers first, then the FMAs
       BSlice<BT, VEC> bs[U][NCH];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const BT* brow = B + size_t(cv[min(t + u, cnt - 1)].x) * N;
+        const size_t roff = size_t(cv[t + u].x) * N;
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(brow + coffl[ch]);
+        for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(bl[ch] + roff);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const float v = t + u < cnt ? __int_as_float(cv[t + u].y) : 0.f;  // padded slot adds 0
-        const uint64_t vv = pack_pair(v);
+        const float2 vv = pair(__int_as_float(cv[t + u].y));  // re-read: frees registers
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
-          float b[VEC];
+          FVec<VEC> b;
           bs[u][ch].widen(b);
-          axpy<VEC>(acc[ch], v, vv, b);
+          acc[ch].fma(vv, b);
+        }
+      }
+    }
+    if (t < cnt) {  // short last batch: padded slots re-read the last row with value 0
+      BSlice<BT, VEC> bs[U][NCH];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const size_t roff = size_t(cv[min(t + u, cnt - 1)].x) * N;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(bl[ch] + roff);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float2 vv = pair(t + u < cnt ? __int_as_float(cv[t + u].y) : 0.f);
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          FVec<VEC> b;
+          bs[u][ch].widen(b);
+          acc[ch].fma(vv, b);
         }
       }
     }
