@@ -65,6 +65,7 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
   Launch L{};
   L.M = plan->M;
   L.N = plan->N;
+  L.K = K;
   L.nnz = plan->nnz;
   L.rowptr = plan->rowptr;
   L.colind = colind;

@@ -53,7 +53,7 @@ namespace spmm {
 
 // Everything one SpMM launch needs (device pointers).
 struct Launch {
-  int32_t M, N;
+  int32_t M, N, K;
   int64_t nnz;
   const int32_t* rowptr;
   const int32_t* colind;
@@ -96,6 +96,7 @@ cudaError_t launch_partition(const int32_t* rowptr, int32_t M, int64_t nnz, int3
 
 
 constexpr int kDefaultItemsPerCta = 2048;
+
 constexpr int kMaxItemsPerCta = 8192;
 constexpr int kMaxDevices = 64;
 

@@ -88,6 +88,7 @@ extern "C" SPMM_API spmm_status spmm_csr_f32_noalloc(int32_t M, int32_t K, int32
   Launch L{};
   L.M = M;
   L.N = N;
+  L.K = K;
   L.nnz = nnz;
   L.rowptr = rowptr;
   L.colind = colind;
