@@ -14,6 +14,8 @@ Functions
 ---------
 ``build()``            compile the C oracle (idempotent).
 ``spmm_reference``     C and the magnitude sum S for all rows or a row list.
+``sddmm_reference``    the sampled dot products out[p] = C_i . B_j and their bound.
+``fusedmm_reference``  E = (SDDMM values) . D and its bound.
 """
 from __future__ import annotations
 
@@ -53,6 +55,13 @@ def load_library(path: str) -> ctypes.CDLL:
     f.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    g = lib.sddmm_oracle_f64
+    g.restype = ctypes.c_int
+    g.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    h = lib.fusedmm_oracle_f64
+    h.restype = ctypes.c_int
+    h.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
     return lib
 
 
@@ -107,3 +116,47 @@ def spmm_reference(rowptr, colind, vals, B, *, b_dtype="f32", rows=None, with_bo
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return C, S
+
+
+def _check_rc(rc):
+    if rc == -2:
+        raise ValueError("oracle: invalid CSR (decreasing rowptr or column index outside [0, K))")
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+
+
+def sddmm_reference(rowptr, colind, C, B, *, library=None):
+    """(out, S): out[p] = C[i] . B[colind[p]] for each stored p of row i, float64."""
+    rowptr = np.ascontiguousarray(rowptr, dtype=np.int32)
+    colind = np.ascontiguousarray(colind, dtype=np.int32)
+    C = np.ascontiguousarray(C, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    M = len(rowptr) - 1
+    K, N = B.shape
+    if C.shape != (M, N):
+        raise ValueError("C must be M x N with B's width")
+    out = np.empty(len(colind), dtype=np.float64)
+    S = np.empty(len(colind), dtype=np.float64)
+    lib = library if library is not None else _lib()
+    _check_rc(lib.sddmm_oracle_f64(M, K, N, _ptr(rowptr), _ptr(colind), _ptr(C), _ptr(B), _ptr(out), _ptr(S)))
+    return out, S
+
+
+def fusedmm_reference(rowptr, colind, C, B, D, *, library=None, with_values=False):
+    """(E, S[, a]): E = SDDMM(C, B on A's pattern) . D in float64, its bound S, and the values a."""
+    rowptr = np.ascontiguousarray(rowptr, dtype=np.int32)
+    colind = np.ascontiguousarray(colind, dtype=np.int32)
+    C = np.ascontiguousarray(C, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    D = np.ascontiguousarray(D, dtype=np.float32)
+    M = len(rowptr) - 1
+    K, N = B.shape
+    if C.shape != (M, N) or D.shape != (K, N):
+        raise ValueError("C must be M x N and D K x N, with B's width")
+    E = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64)
+    a = np.empty(len(colind), dtype=np.float64)
+    lib = library if library is not None else _lib()
+    _check_rc(lib.fusedmm_oracle_f64(M, K, N, _ptr(rowptr), _ptr(colind), _ptr(C), _ptr(B), _ptr(D),
+                                     _ptr(E), _ptr(S), _ptr(a)))
+    return (E, S, a) if with_values else (E, S)

@@ -89,3 +89,70 @@ int spmm_oracle_rows_f64(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
   }
   return 0;
 }
+
+/*
+ * SDDMM (page "Performance Optimization of Deep Learning Sparse Matrix
+ * Kernels on Intel Max Series GPU", SDDMM section, Algorithm 1, Figs. 3-4):
+ * the dense product C . B^T is computed only where A has a stored entry; the
+ * entry (i, j) receives the dot product of row i of C (M x N) and row j of B
+ * (K x N).  A's stored values are not used (the page stores the products into
+ * A).  out[p] for every stored position p; S_out[p] = sum_n |C[i][n] B[j][n]|.
+ * Returns 0, -1 on a size error, -2 on malformed CSR (as above).
+ */
+int sddmm_oracle_f64(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, const int32_t* colind,
+                     const float* C, const float* B, double* out, double* S_out) {
+  if (M < 0 || K < 0 || N < 0 || !rowptr || !out) return -1;
+  for (int32_t i = 0; i < M; ++i) {
+    if (rowptr[i + 1] < rowptr[i]) return -2;
+    for (int64_t p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+      const int64_t j = colind[p];
+      if (j < 0 || j >= K) return -2;
+      double dot = 0.0, mag = 0.0;
+      for (int32_t n = 0; n < N; ++n) {
+        const double prod = (double)C[(int64_t)i * N + n] * (double)B[j * N + n];
+        dot += prod;
+        mag += fabs(prod);
+      }
+      out[p] = dot;
+      if (S_out) S_out[p] = mag;
+    }
+  }
+  return 0;
+}
+
+/*
+ * FusedMM (same page, FusedMM section, Fig. 6, Algorithm 3, Fig. 11): row by
+ * row, the SDDMM values a_ij = C_i . B_j of the row's stored positions are
+ * computed and, without being stored, used at once as the sparse values of an
+ * SpMM with a third dense matrix D (K x N): E_i = sum_j a_ij D_j.  Inputs are
+ * the pattern (rowptr, colind), C, B and D; the output is E (M x N).
+ * S_out[i][n] = sum_j |a_ij| |D_j[n]|, with a_ij exact, bounds the SpMM half;
+ * A_out (nullable) receives the a_ij values in CSR order.
+ */
+int fusedmm_oracle_f64(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, const int32_t* colind,
+                       const float* C, const float* B, const float* D, double* E_out, double* S_out,
+                       double* A_out) {
+  if (M < 0 || K < 0 || N < 0 || !rowptr || !E_out) return -1;
+  for (int32_t i = 0; i < M; ++i) {
+    double* e = E_out + (int64_t)i * N;
+    double* s = S_out ? S_out + (int64_t)i * N : NULL;
+    for (int32_t n = 0; n < N; ++n) {
+      e[n] = 0.0;
+      if (s) s[n] = 0.0;
+    }
+    if (rowptr[i + 1] < rowptr[i]) return -2;
+    for (int64_t p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+      const int64_t j = colind[p];
+      if (j < 0 || j >= K) return -2;
+      double a = 0.0;
+      for (int32_t n = 0; n < N; ++n) a += (double)C[(int64_t)i * N + n] * (double)B[j * N + n];
+      if (A_out) A_out[p] = a;
+      for (int32_t n = 0; n < N; ++n) {
+        const double prod = a * (double)D[j * N + n];
+        e[n] += prod;
+        if (s) s[n] += fabs(prod);
+      }
+    }
+  }
+  return 0;
+}
