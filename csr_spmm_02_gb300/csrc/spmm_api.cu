@@ -91,6 +91,61 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
   return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
 }
 
+Launch plan_launch(spmm_plan_t plan, cudaStream_t stream) {
+  Launch L{};
+  L.M = plan->M;
+  L.N = plan->N;
+  L.nnz = plan->nnz;
+  L.rowptr = plan->rowptr;
+  L.part = plan->part;
+  L.num_ctas = plan->num_ctas;
+  L.items_per_cta = plan->items_per_cta;
+  L.carry = plan->carry;
+  L.err = plan->err;
+  L.stream = stream;
+  return L;
+}
+
+spmm_status sddmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* Cd, const float* B, float* out,
+                  cudaStream_t stream) {
+  if (!plan) return SPMM_ERR_PLAN_MISMATCH;
+  if (K < 0) return SPMM_ERR_INVALID_ARG;
+  if (plan->nnz == 0) return SPMM_OK;
+  if (!out || !colind) return SPMM_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return SPMM_ERR_CUDA;
+  if (plan->N == 0)  // empty dot products
+    return cudaMemsetAsync(out, 0, size_t(plan->nnz) * sizeof(float), stream) == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+  if (!Cd || !B || K == 0) return SPMM_ERR_INVALID_ARG;
+  const bool vector_ok = plan->N % 4 == 0 && aligned16(B) && aligned16(Cd);
+  Launch L = plan_launch(plan, stream);
+  L.K = K;
+  L.colind = colind;
+  L.B = B;
+  const cudaError_t e = launch_sddmm_f32(L, choose_shape_balanced(plan->N, false, vector_ok), Cd, out);
+  return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+}
+
+spmm_status fusedmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* Cd, const float* B,
+                    const float* D, float* E, cudaStream_t stream) {
+  if (!plan) return SPMM_ERR_PLAN_MISMATCH;
+  if (K < 0) return SPMM_ERR_INVALID_ARG;
+  if (plan->M == 0 || plan->N == 0) return SPMM_OK;
+  if (!E || (plan->nnz > 0 && (!colind || !Cd || !B || !D || K == 0))) return SPMM_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return SPMM_ERR_CUDA;
+  const bool vector_ok = plan->N % 4 == 0 && aligned16(B) && aligned16(Cd) && aligned16(D) && aligned16(E);
+  Launch L = plan_launch(plan, stream);
+  L.K = K;
+  L.colind = colind;
+  L.B = D;  // gathered and accumulated
+  L.C = E;
+  cudaError_t e = launch_fusedmm_f32(L, choose_shape_balanced(plan->N, false, vector_ok), Cd, B);
+  if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+  if (e == cudaSuccess) e = launch_fixup(L);
+  return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+}
+
 spmm_status one_call(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, const int32_t* colind,
                      const float* vals, const void* B, bool bf16, float* C, void* stream) {
   if (M < 0 || K < 0 || N < 0) return SPMM_ERR_INVALID_ARG;
@@ -133,6 +188,16 @@ spmm_status spmm_csr_f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
 spmm_status spmm_csr_bf16f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, const int32_t* colind,
                              const float* vals, const uint16_t* B, float* C, void* stream) {
   return one_call(M, K, N, rowptr, colind, vals, B, true, C, stream);
+}
+
+spmm_status spmm_csr_sddmm_f32(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* C, const float* B,
+                               float* out, void* stream) {
+  return sddmm(plan, K, colind, C, B, out, static_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_csr_fusedmm_f32(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* C,
+                                 const float* B, const float* D, float* E, void* stream) {
+  return fusedmm(plan, K, colind, C, B, D, E, static_cast<cudaStream_t>(stream));
 }
 
 spmm_status spmm_plan_set_split_event(spmm_plan_t plan, void* event) {

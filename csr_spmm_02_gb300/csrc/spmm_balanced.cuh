@@ -34,6 +34,11 @@
 //     lie inside the CTA go to C, the CTA's first and last rows to its carry
 //     slots 0 and 1, which the fixup kernel adds across CTAs in CTA order.
 //
+// FusedMM mode (same page, FusedMM section, Fig. 6, Algorithm 3, Fig. 11):
+// the sparse value of each nonzero (i, j) is not read from vals but computed
+// as the SDDMM dot product C_i . B_j of two dense fp32 matrices, and the
+// gathered rows belong to a third matrix D; the values are never stored.
+//
 // No floating-point atomics anywhere, so C is bitwise reproducible for a given
 // plan.
 #pragma once
@@ -42,6 +47,7 @@
 
 #include "spmm_device.cuh"
 #include "spmm_internal.h"
+#include "spmm_sddmm.cuh"
 
 #ifndef SPMM_BAL_LOADS
 #define SPMM_BAL_LOADS 8  // 16-byte B loads in flight per lane (U steps x NCH chunks)
@@ -75,13 +81,16 @@ __host__ __device__ constexpr size_t balanced_smem_layout_bytes(int W, int TW, i
          + 16;                     // mbarrier
 }
 
-template <typename BT, int VEC, int G, int NCH>
+template <typename BT, int VEC, int G, int NCH, bool FUSED>
 __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
     spmm_balanced_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr,
                          const int32_t* __restrict__ colind, const float* __restrict__ vals,
                          const BT* __restrict__ B, float* __restrict__ C,
                          const int2* __restrict__ part, int32_t T, float* __restrict__ carry,
-                         int* __restrict__ err) {
+                         int* __restrict__ err, const float* __restrict__ Cd, const float* __restrict__ Bd) {
+  // FUSED: B is D (gathered and accumulated), Cd and Bd the SDDMM operands, vals unused.
+  static_assert(!FUSED || sizeof(BT) == 4, "FusedMM is fp32");
+  using DotSlice = BSlice<float, FUSED ? VEC : 1>;  // fp32 slices of the dot-product operands
   constexpr int S = 32 / G;                // nonzeros per warp step
   constexpr int W = kThreads / 32;         // warps (workers) per CTA
   constexpr int TW = G * VEC * NCH;        // columns per tile
@@ -117,10 +126,11 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
   for (int k = tid; k < W; k += kThreads) s_meta[k] = make_int2(-1, 0);
   __syncthreads();
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar, (c_bulk ? 8u * uint32_t(cb - ca) : 0u) + (r_bulk ? 4u * uint32_t(rb - ra) : 0u));
+    mbar_arrive_expect_tx(bar, (c_bulk ? (FUSED ? 4u : 8u) * uint32_t(cb - ca) : 0u) +
+                                   (r_bulk ? 4u * uint32_t(rb - ra) : 0u));
     if (c_bulk) {
       bulk_g2s(smem_addr(s_col + (ca - nbase)), colind + ca, 4u * uint32_t(cb - ca), bar);
-      bulk_g2s(smem_addr(s_val + (ca - nbase)), vals + ca, 4u * uint32_t(cb - ca), bar);
+      if (!FUSED) bulk_g2s(smem_addr(s_val + (ca - nbase)), vals + ca, 4u * uint32_t(cb - ca), bar);
     }
     if (r_bulk) bulk_g2s(smem_addr(s_rp + (ra - rbase)), rowptr + ra, 4u * uint32_t(rb - ra), bar);
   }
@@ -128,12 +138,12 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
     const int g = tid < 4 ? p0 + tid : cb + (tid - 4);
     if (tid < 8 && ((tid < 4 && g < ca) || (tid >= 4 && g < p1))) {
       s_col[g - nbase] = ld_stream(colind + g, stream_pol);
-      s_val[g - nbase] = ld_stream(vals + g, stream_pol);
+      if (!FUSED) s_val[g - nbase] = ld_stream(vals + g, stream_pol);
     }
   } else {
     for (int g = p0 + tid; g < p1; g += kThreads) {
       s_col[g - nbase] = ld_stream(colind + g, stream_pol);
-      s_val[g - nbase] = ld_stream(vals + g, stream_pol);
+      if (!FUSED) s_val[g - nbase] = ld_stream(vals + g, stream_pol);
     }
   }
   if (r_bulk) {
@@ -180,6 +190,52 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
   }
   const int* colw = s_col - nbase + grp;  // colw[a] = colind of nonzero a + grp (staged)
   const float* valw = s_val - nbase + grp;
+  // FusedMM: dot-product operands of this lane (first column tile of C and Bd),
+  // the row of the group's current nonzero, and that row's C slice.
+  int dcoff[NCH];
+  bool dvalid[NCH];
+  const float* bdl[NCH];
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int col = (ch * G + gl) * VEC;
+    dvalid[ch] = col < N;
+    dcoff[ch] = min(col, N - VEC);
+    bdl[ch] = FUSED ? Bd + dcoff[ch] : nullptr;
+  }
+  const int last_row = i1 - i0;
+  int rg = rw0, loaded = -1;
+  FVec<VEC> cfr[FUSED ? NCH : 1];
+  // Group sums of the dot products of the U steps starting at q (all lanes take part).
+  auto fused_values = [&](int q, const DotSlice (&bd)[FUSED ? BalancedSteps<NCH>::value : 1][NCH],
+                          float (&v)[FUSED ? BalancedSteps<NCH>::value : 1]) {
+    if constexpr (FUSED) {
+#pragma unroll
+      for (int s = 0; s < U; ++s) {
+        const int n = q + s * S + grp;
+        float d = 0.f;
+        if (n < pw1) {
+          while (rg < last_row && rp[rg + 1] <= n) ++rg;
+          if (rg != loaded) {
+            const float* crow = Cd + size_t(i0 + rg) * N;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              DotSlice t;
+              t.load(crow + dcoff[ch]);
+              t.widen(cfr[ch]);
+            }
+            loaded = rg;
+          }
+          FVec<VEC> b[NCH];
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) bd[s][ch].widen(b[ch]);
+          d = dot_lane<VEC, NCH>(cfr, b, dvalid, 0.f);
+          if (N > G * VEC * NCH)
+            d = dot_tail_tiles<VEC, G, NCH>(Cd + size_t(i0 + rg) * N, Bd + size_t(colw[q + s * S]) * N, N, gl, d);
+        }
+        v[s] = group_sum<G>(d);
+      }
+    }
+  };
   auto slot_ptr = [&](int worker, int ch) { return s_slot + worker * TW + (ch * G + gl) * VEC; };
   FVec<VEC> acc[NCH];
 #pragma unroll
@@ -247,16 +303,25 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
   int q = pw0;
   for (; q + U * S <= pw1; q += U * S) {  // full batches
     BSlice<BT, VEC> bs[U][NCH];
+    DotSlice bd[FUSED ? U : 1][NCH];
+    float fv[FUSED ? U : 1];
 #pragma unroll
     for (int s = 0; s < U; ++s) {  // gathers first
       const size_t roff = size_t(colw[q + s * S]) * N;
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
+      for (int ch = 0; ch < NCH; ++ch) {
+        bs[s][ch].load(bl[ch] + roff);
+        if constexpr (FUSED) bd[s][ch].load(bdl[ch] + roff);
+      }
     }
+    fused_values(q, bd, fv);
+    auto value = [&](int s) {
+      if constexpr (FUSED) return fv[s]; else return valw[q + s * S];
+    };
     if (next_end > q + U * S) {  // no row ends inside the batch
 #pragma unroll
       for (int s = 0; s < U; ++s) {
-        const float2 vv = pair(valw[q + s * S]);
+        const float2 vv = pair(value(s));
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           FVec<VEC> b;
@@ -266,22 +331,30 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
       }
     } else {
 #pragma unroll
-      for (int s = 0; s < U; ++s) step(q + s * S, valw[q + s * S], bs[s]);
+      for (int s = 0; s < U; ++s) step(q + s * S, value(s), bs[s]);
     }
   }
   if (q < pw1) {  // short last batch: slots past the sub-range re-read its last nonzero's row, value 0
     BSlice<BT, VEC> bs[U][NCH];
+    DotSlice bd[FUSED ? U : 1][NCH];
+    float fv[FUSED ? U : 1];
 #pragma unroll
     for (int s = 0; s < U; ++s) {
       const size_t roff = size_t(colw[min(q + s * S, pw1 - 1 - grp)]) * N;
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
+      for (int ch = 0; ch < NCH; ++ch) {
+        bs[s][ch].load(bl[ch] + roff);
+        if constexpr (FUSED) bd[s][ch].load(bdl[ch] + roff);
+      }
     }
+    fused_values(q, bd, fv);
 #pragma unroll
     for (int s = 0; s < U; ++s) {
       const int a = q + s * S;
       if (a >= pw1) break;
-      step(a, a + grp < pw1 ? valw[a] : 0.f, bs[s]);
+      float v;
+      if constexpr (FUSED) v = fv[s]; else v = a + grp < pw1 ? valw[a] : 0.f;
+      step(a, v, bs[s]);
     }
   }
   while (r < rw1) end_row();  // rows ending exactly at the sub-range end (empty rows too)
@@ -326,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
   }
 }
 
-template <typename BT, int VEC, int G, int NCH>
-cudaError_t launch_balanced_t(const Launch& L) {
+template <typename BT, int VEC, int G, int NCH, bool FUSED = false>
+cudaError_t launch_balanced_t(const Launch& L, const float* Cd = nullptr, const float* Bd = nullptr) {
   constexpr int W = kThreads / 32;
   constexpr int TW = G * VEC * NCH;
   const size_t smem = balanced_smem_layout_bytes(W, TW, L.items_per_cta);
@@ -336,15 +409,15 @@ cudaError_t launch_balanced_t(const Launch& L) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= kMaxDevices || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(spmm_balanced_kernel<BT, VEC, G, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(spmm_balanced_kernel<BT, VEC, G, NCH, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(balanced_smem_layout_bytes(W, TW, kMaxItemsPerCta)));
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
   const dim3 grid(unsigned(L.num_ctas), unsigned((L.N + TW - 1) / TW));
-  spmm_balanced_kernel<BT, VEC, G, NCH><<<grid, kThreads, smem, L.stream>>>(
+  spmm_balanced_kernel<BT, VEC, G, NCH, FUSED><<<grid, kThreads, smem, L.stream>>>(
       L.M, L.N, L.rowptr, L.colind, L.vals, static_cast<const BT*>(L.B), L.C, L.part,
-      L.items_per_cta, L.carry, L.err);
+      L.items_per_cta, L.carry, L.err, Cd, Bd);
   return cudaGetLastError();
 }
 

@@ -90,6 +90,8 @@ cudaError_t launch_row_bf16(const Launch& L, Shape s);
 cudaError_t launch_balanced_f32(const Launch& L, Shape s);
 cudaError_t launch_balanced_bf16(const Launch& L, Shape s);
 cudaError_t launch_fixup(const Launch& L);
+cudaError_t launch_sddmm_f32(const Launch& L, Shape s, const float* Cd, float* out);
+cudaError_t launch_fusedmm_f32(const Launch& L, Shape s, const float* Cd, const float* Bd);
 // Merge-path coordinates of the P+1 range starts (ranges of T items) into part.
 cudaError_t launch_partition(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t T, int32_t P, int2* part,
                              cudaStream_t stream);

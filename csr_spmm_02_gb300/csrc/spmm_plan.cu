@@ -188,7 +188,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
     plan->kernel = double(plan->max_row_nnz) <= 4.0 * mean + 32.0 ? SPMM_KERNEL_ROW : SPMM_KERNEL_BALANCED;
   }
 
-  if (plan->kernel == SPMM_KERNEL_BALANCED) {
+  {  // merge-path partition and carry rows: used by the balanced SpMM, SDDMM and FusedMM
     const int T = items_per_cta ? items_per_cta : kDefaultItemsPerCta;
     const int64_t total = int64_t(M) + nnz;
     const int64_t P = (total + T - 1) / T;

@@ -37,7 +37,7 @@ KERNEL_NAMES = {1: "row", 2: "balanced"}
 EXPORTS = ["spmm_csr_plan", "spmm_csr_plan_ex", "spmm_plan_get_info", "spmm_plan_destroy",
            "spmm_csr_f32_exec", "spmm_csr_bf16f32_exec", "spmm_csr_f32", "spmm_csr_bf16f32",
            "spmm_csr_validate", "spmm_plan_check_device", "spmm_plan_set_split_event",
-           "spmm_csr_f32_noalloc", "spmm_status_string"]
+           "spmm_csr_f32_noalloc", "spmm_csr_sddmm_f32", "spmm_csr_fusedmm_f32", "spmm_status_string"]
 
 
 class SpmmError(RuntimeError):
@@ -83,6 +83,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "spmm_plan_check_device": [vp, vp],
         "spmm_plan_set_split_event": [vp, vp],
         "spmm_csr_f32_noalloc": [i32, i32, i32, i64, vp, vp, vp, vp, vp, vp],
+        "spmm_csr_sddmm_f32": [vp, i32, vp, vp, vp, vp, vp],
+        "spmm_csr_fusedmm_f32": [vp, i32, vp, vp, vp, vp, vp, vp],
         "spmm_status_string": [ctypes.c_int],
     }
     for name, args in sig.items():
@@ -184,6 +186,22 @@ def spmm_csr_bf16f32(M, K, N, rowptr, colind, vals, B, C, stream=None):
                                    _ptr(vals, _F32, "vals", True), _ptr(B, _BF16_BITS, "B", True),
                                    _ptr(C, _F32, "C"), _stream(stream)), "spmm_csr_bf16f32")
     return C
+
+
+def spmm_csr_sddmm_f32(plan: Plan, K, colind, C, B, out, stream=None):
+    """out[p] = C[i] . B[colind[p]] on A's pattern (fp32)."""
+    _check(load().spmm_csr_sddmm_f32(plan.handle, K, _ptr(colind, _I32, "colind", True), _ptr(C, _F32, "C", True),
+                                     _ptr(B, _F32, "B", True), _ptr(out, _F32, "out", True), _stream(stream)),
+           "spmm_csr_sddmm_f32")
+    return out
+
+
+def spmm_csr_fusedmm_f32(plan: Plan, K, colind, C, B, D, E, stream=None):
+    """E = SDDMM(C, B on A's pattern) . D without storing the SDDMM values (fp32)."""
+    _check(load().spmm_csr_fusedmm_f32(plan.handle, K, _ptr(colind, _I32, "colind", True), _ptr(C, _F32, "C", True),
+                                       _ptr(B, _F32, "B", True), _ptr(D, _F32, "D", True), _ptr(E, _F32, "E"),
+                                       _stream(stream)), "spmm_csr_fusedmm_f32")
+    return E
 
 
 def spmm_csr_f32_noalloc(M, K, N, nnz, rowptr, colind, vals, B, C, stream=None):

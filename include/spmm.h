@@ -124,7 +124,8 @@ SPMM_API spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t 
                              int32_t kernel, int32_t items_per_cta, void* stream,
                              spmm_plan_t* plan_out);
 
-/* Copy the plan's decisions into *info (host memory). */
+/* Copy the plan's decisions into *info (host memory).  Every plan also holds
+ * the merge-path partition used by the balanced SpMM, SDDMM and FusedMM. */
 SPMM_API spmm_status spmm_plan_get_info(spmm_plan_t plan, spmm_plan_info* info);
 
 /* Free the plan and its workspace (synchronous). NULL is accepted. */
@@ -142,6 +143,28 @@ SPMM_API spmm_status spmm_csr_f32_exec(spmm_plan_t plan, int32_t K, const int32_
 SPMM_API spmm_status spmm_csr_bf16f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind,
                                   const float* vals, const uint16_t* B, float* C,
                                   void* stream);
+
+/*
+ * SDDMM on A's pattern (page "Performance Optimization of Deep Learning Sparse
+ * Matrix Kernels on Intel Max Series GPU", SDDMM section, Algorithm 1):
+ * out[p] = sum_n C[i][n] * B[colind[p]][n] for every stored position p of
+ * row i.  A's values are not used.  C is M x N, B is K x N (fp32, row-major,
+ * N the plan's width); out is fp32[nnz] in CSR order.  Uses the plan's row
+ * partition; asynchronous on `stream`; every output written once, so results
+ * are deterministic.  Tolerance-wise each value is an fp32 dot product.
+ */
+SPMM_API spmm_status spmm_csr_sddmm_f32(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* C,
+                                        const float* B, float* out, void* stream);
+
+/*
+ * FusedMM (same page, FusedMM section, Fig. 6, Algorithm 3, Fig. 11):
+ * E[i] = sum over stored j of row i of (C[i] . B[j]) * D[j], the SDDMM values
+ * used at once as the sparse values of an SpMM and never stored.  C is M x N,
+ * B and D are K x N, E is M x N (fp32, row-major, N the plan's width).  Runs
+ * the nnz-balanced kernel and its fixup; deterministic for a given plan.
+ */
+SPMM_API spmm_status spmm_csr_fusedmm_f32(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* C,
+                                          const float* B, const float* D, float* E, void* stream);
 
 /*
  * One-call form: plans, multiplies and frees on `stream`.  Plan workspace is

@@ -1,0 +1,159 @@
+"""SDDMM and FusedMM on the GPU vs the CPU oracle, through the C ABI.
+
+Bounds: an SDDMM value is an fp32 dot product, |out - ref| <= 1e-5 * S + 1e-30
+with S = sum_n |C_in B_jn|.  FusedMM's values carry that dot-product error into
+E, so its bound uses the magnitudes of the whole computation,
+S_f[i, n] = sum_j S_ij |D_jn| (the SDDMM bound times |D|), computed with the
+oracles."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from csr_spmm_02_gb300 import gen, spmm
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+def problem(seed, M=1200, K=800, N=64, integer=False):
+    rng = np.random.default_rng(seed)
+    p = gen.random_csr(rng, M, K, N, mean_row=9, empty_frac=0.3, long_rows=[(5, K), (M - 2, 700)])
+    if integer:
+        C = rng.integers(-2, 3, (M, N)).astype(np.float32)
+        B = rng.integers(-2, 3, (K, N)).astype(np.float32)
+        D = rng.integers(-2, 3, (K, N)).astype(np.float32)
+    else:
+        C = rng.uniform(-1, 1, (M, N)).astype(np.float32)
+        B = rng.uniform(-1, 1, (K, N)).astype(np.float32)
+        D = rng.uniform(-1, 1, (K, N)).astype(np.float32)
+    return p, C, B, D
+
+
+def run_sddmm(p, C, B, T=256, arrays=None):
+    a = arrays or H.device_arrays(p)
+    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N, items_per_cta=T)
+    out = torch.full((p.nnz,), float("nan"), device="cuda")
+    spmm.spmm_csr_sddmm_f32(plan, p.K, a["colind"], torch.from_numpy(C).cuda(), torch.from_numpy(B).cuda(), out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64)
+
+
+def run_fusedmm(p, C, B, D, T=256, arrays=None):
+    a = arrays or H.device_arrays(p)
+    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N, items_per_cta=T)
+    E = torch.full((p.M, p.N), float("nan"), device="cuda")
+    spmm.spmm_csr_fusedmm_f32(plan, p.K, a["colind"], torch.from_numpy(C).cuda(), torch.from_numpy(B).cuda(),
+                              torch.from_numpy(D).cuda(), E)
+    torch.cuda.synchronize()
+    assert spmm.spmm_plan_check_device(plan) == 0
+    return E.cpu().numpy().astype(np.float64)
+
+
+def fused_bound(p, C, B, D):
+    _, S = oracle.sddmm_reference(p.rowptr, p.colind, C, B)
+    Sf, _ = oracle.spmm_reference(p.rowptr, p.colind, S.astype(np.float32), np.abs(D))
+    return Sf
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 8, 32, 33, 64, 128, 130, 256, 600])
+def test_sddmm_parity(N):
+    p, C, B, _ = problem(N, N=N)
+    got = run_sddmm(p, C, B)
+    ref, S = oracle.sddmm_reference(p.rowptr, p.colind, C, B)
+    assert np.all(np.abs(got - ref) <= 1e-5 * S + 1e-30)
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 8, 32, 33, 64, 128, 130, 256, 600])
+def test_fusedmm_parity(N):
+    p, C, B, D = problem(100 + N, N=N)
+    got = run_fusedmm(p, C, B, D)
+    ref, _ = oracle.fusedmm_reference(p.rowptr, p.colind, C, B, D)
+    H.assert_within(got, ref, fused_bound(p, C, B, D), "f32", f"fusedmm N={N}")
+
+
+@pytest.mark.parametrize("N", [8, 64])
+def test_integer_exact(N):
+    p, C, B, D = problem(200 + N, N=N, integer=True)
+    ref, _ = oracle.sddmm_reference(p.rowptr, p.colind, C, B)
+    assert np.array_equal(run_sddmm(p, C, B), ref)
+    ref, _ = oracle.fusedmm_reference(p.rowptr, p.colind, C, B, D)
+    assert np.array_equal(run_fusedmm(p, C, B, D), ref)
+
+
+def test_deterministic_and_range_sizes():
+    p, C, B, D = problem(7, N=32)
+    a = H.device_arrays(p)
+    e1, e2 = run_fusedmm(p, C, B, D, arrays=a), run_fusedmm(p, C, B, D, arrays=a)
+    assert np.array_equal(e1, e2)
+    ref, _ = oracle.fusedmm_reference(p.rowptr, p.colind, C, B, D)
+    Sf = fused_bound(p, C, B, D)
+    for T in (512, 2048, 8192):
+        H.assert_within(run_fusedmm(p, C, B, D, T=T, arrays=a), ref, Sf, "f32", f"T={T}")
+        out = run_sddmm(p, C, B, T=T, arrays=a)
+        sref, S = oracle.sddmm_reference(p.rowptr, p.colind, C, B)
+        assert np.all(np.abs(out - sref) <= 1e-5 * S + 1e-30)
+
+
+def test_scalar_path_misaligned():
+    p, C, B, D = problem(9, N=64)
+    a = H.device_arrays(p)
+    def shifted(x):
+        t = torch.from_numpy(x).cuda().reshape(-1)
+        buf = torch.empty(t.numel() + 1, device="cuda")
+        buf[1:].copy_(t)
+        return buf[1:].view(x.shape)
+    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N, items_per_cta=256)
+    out = torch.empty(p.nnz, device="cuda")
+    spmm.spmm_csr_sddmm_f32(plan, p.K, a["colind"], shifted(C), shifted(B), out)
+    Ebuf = torch.empty(p.M * p.N + 1, device="cuda")
+    E = Ebuf[1:].view(p.M, p.N)
+    spmm.spmm_csr_fusedmm_f32(plan, p.K, a["colind"], shifted(C), shifted(B), shifted(D), E)
+    torch.cuda.synchronize()
+    ref, S = oracle.sddmm_reference(p.rowptr, p.colind, C, B)
+    assert np.all(np.abs(out.cpu().numpy() - ref) <= 1e-5 * S + 1e-30)
+    Eref, _ = oracle.fusedmm_reference(p.rowptr, p.colind, C, B, D)
+    H.assert_within(E, Eref, fused_bound(p, C, B, D), "f32", "fusedmm misaligned")
+
+
+def test_empty_pattern():
+    M, K, N = 50, 20, 16
+    p = gen.CsrProblem("empty", M, K, N, np.zeros(M + 1, np.int32), np.zeros(0, np.int32), np.zeros(0, np.float32),
+                       np.zeros((K, N), np.float32), "f32")
+    a = H.device_arrays(p)
+    plan = spmm.spmm_csr_plan(a["rowptr"], M, 0, N)
+    E = torch.full((M, N), float("nan"), device="cuda")
+    z = torch.zeros((K, N), device="cuda")
+    spmm.spmm_csr_fusedmm_f32(plan, K, None, torch.zeros((M, N), device="cuda"), z, z, E)
+    torch.cuda.synchronize()
+    assert not bool(E.any()) and bool(torch.isfinite(E).all())
+
+
+@pytest.mark.parametrize("name", ["uniform64k", "rmat22"])
+def test_workload_structures(name):
+    """Full-size patterns of two benchmark workloads (N of the workload), sampled outputs."""
+    p = gen.make_workload(name)
+    rng = np.random.default_rng(5)
+    C = rng.uniform(-1, 1, (p.M, p.N)).astype(np.float32)
+    D = rng.uniform(-1, 1, (p.K, p.N)).astype(np.float32)
+    B = p.B
+    a = H.device_arrays(p)
+    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N)
+    Cd, Bd, Dd = (torch.from_numpy(x).cuda() for x in (C, B, D))
+    out = torch.empty(p.nnz, device="cuda")
+    spmm.spmm_csr_sddmm_f32(plan, p.K, a["colind"], Cd, Bd, out)
+    E = torch.empty((p.M, p.N), device="cuda")
+    spmm.spmm_csr_fusedmm_f32(plan, p.K, a["colind"], Cd, Bd, Dd, E)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.argsort(np.diff(p.rowptr))[-32:], rng.choice(p.M, 3000, replace=False)]))
+    sub = gen.CsrProblem("sub", len(rows), p.K, p.N,
+                         np.concatenate([[0], np.cumsum(np.diff(p.rowptr)[rows])]).astype(np.int32),
+                         np.concatenate([p.colind[p.rowptr[r]:p.rowptr[r + 1]] for r in rows]).astype(np.int32),
+                         np.zeros(0, np.float32), B, "f32")
+    sub.vals = np.zeros(len(sub.colind), np.float32)
+    Csub = C[rows]
+    ref, S = oracle.sddmm_reference(sub.rowptr, sub.colind, Csub, B)
+    got = np.concatenate([out[int(p.rowptr[r]):int(p.rowptr[r + 1])].cpu().numpy() for r in rows]).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 1e-5 * S + 1e-30)
+    Eref, _ = oracle.fusedmm_reference(sub.rowptr, sub.colind, Csub, B, D)
+    H.assert_within(E[torch.from_numpy(rows).cuda()], Eref, fused_bound(sub, Csub, B, D), "f32", name)
