@@ -1,10 +1,11 @@
 #!/usr/bin/env python
 """SpMM benchmark: GFLOP/s (2*nnz*N / time) and effective HBM GB/s.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--op spmm|sddmm|fusedmm]
                     [--impl ours|reference]
 
-One step is one C = A . B over one of the seeded synthetic workloads
+One step is one C = A . B (or, with --op, one SDDMM or FusedMM on the same
+sparsity pattern) over one of the seeded synthetic workloads
 (default ``uniform64k``: M=K=65536, 32 random columns per row, N=64, fp32),
 through the C ABI with a plan built once before timing (the plan is the
 per-structure preprocessing; its time is reported as ``config.plan_ms``).
@@ -40,6 +41,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "SpMM GFLOP/s (2*nnz*N/s) and effective HBM GB/s vs peak, 1xGB300"
+OP_METRIC = {
+    "spmm": METRIC,
+    "sddmm": "SDDMM GFLOP/s (2*nnz*N/s) and effective HBM GB/s vs peak, 1xGB300",
+    "fusedmm": "FusedMM GFLOP/s (4*nnz*N/s) and effective HBM GB/s vs peak, 1xGB300",
+}
 UNIT = "GFLOP/s"
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
@@ -174,6 +180,38 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+# the three operations on a workload's pattern
+# ----------------------------------------------------------------------------
+def op_flops(p, op):
+    return (4 if op == "fusedmm" else 2) * p.nnz * p.N
+
+
+def op_bytes(p, op):
+    """Compulsory bytes: every input read once, every output written once."""
+    if op == "spmm":
+        return p.compulsory_bytes()
+    pattern = 4 * (p.M + 1) + 4 * p.nnz
+    dense = 4 * p.M * p.N + 4 * p.K * p.N  # C and B (fp32)
+    if op == "sddmm":
+        return pattern + dense + 4 * p.nnz
+    return pattern + dense + 4 * p.K * p.N + 4 * p.M * p.N  # + D, E
+
+
+def op_dense_inputs(p, op):
+    """fp32 operands of SDDMM / FusedMM on the workload's pattern: (C, B, D).
+
+    B is the workload's B (widened exactly to fp32 where it is stored as
+    bf16); C (M x N) and D (K x N) are seeded uniform(-1, 1)."""
+    import numpy as np
+    from csr_spmm_02_gb300 import gen
+    rng = np.random.default_rng(1000 + (p.seed or 0))
+    C = gen.dense_f32(rng, p.M, p.N)
+    D = gen.dense_f32(rng, p.K, p.N) if op == "fusedmm" else None
+    B = p.B if p.b_dtype == "f32" else (p.B.astype(np.uint32) << 16).view(np.float32)
+    return C, B, D
+
+
+# ----------------------------------------------------------------------------
 # CPU oracle timing (the CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------
 def oracle_rows_block(p, start, count):
@@ -181,7 +219,7 @@ def oracle_rows_block(p, start, count):
     return np.arange(start, start + count, dtype=np.int32)
 
 
-def time_oracle(p, seconds: float):
+def time_oracle(p, seconds: float, op="spmm", dense=None):
     """Run the oracle over consecutive row blocks (wrapping) for ~`seconds`.
 
     Returns (GFLOP/s, description of the sample)."""
@@ -195,22 +233,46 @@ def time_oracle(p, seconds: float):
     rows_done = 0
     while spent < seconds:
         count = min(block, p.M - start)
-        rows = oracle_rows_block(p, start, count)
         t0 = time.perf_counter()
-        oracle.spmm_reference(p.rowptr, p.colind, p.vals, p.B, b_dtype=p.b_dtype, rows=rows, with_bound=False)
+        if op == "spmm":
+            rows = oracle_rows_block(p, start, count)
+            oracle.spmm_reference(p.rowptr, p.colind, p.vals, p.B, b_dtype=p.b_dtype, rows=rows, with_bound=False)
+        else:
+            rp = p.rowptr[start:start + count + 1]
+            ci = p.colind[int(rp[0]):int(rp[-1])]
+            rp = (rp - rp[0]).astype(np.int32)
+            C, B, D = dense
+            if op == "sddmm":
+                oracle.sddmm_reference(rp, ci, C[start:start + count], B)
+            else:
+                oracle.fusedmm_reference(rp, ci, C[start:start + count], B, D)
         spent += time.perf_counter() - t0
-        flops += 2.0 * float(lens[start:start + count].sum()) * p.N
+        flops += (4.0 if op == "fusedmm" else 2.0) * float(lens[start:start + count].sum()) * p.N
         rows_done += count
         start = (start + count) % p.M
-    desc = (f"oracle over {rows_done} rows (consecutive blocks of {block} rows from row 0, wrapping; "
-            f"{flops / 2 / p.N:.0f} nonzeros x N={p.N}) in {spent:.2f} s, single thread")
-    return flops / spent / 1e9, desc
+    desc = (f"{op} oracle over {rows_done} rows (consecutive blocks of {block} rows from row 0, wrapping; "
+            f"{flops / (4 if op == 'fusedmm' else 2) / p.N:.0f} nonzeros x N={p.N}) in {spent:.2f} s, single thread")
+    return flops / spent / 1e9, desc, spent
 
 
 def reference_arm(args, p, cfg):
     """--impl reference: the CPU oracle, K timed steps of a bounded sample each."""
     import numpy as np
     import oracle
+    if args.op != "spmm":
+        steps = args.steps if args.steps is not None else 3
+        dense = op_dense_inputs(p, args.op)
+        runs = [time_oracle(p, 0.5, args.op, dense) for _ in range(max(args.warmup, 0) + steps)][args.warmup:]
+        value = sum(r[0] for r in runs) / len(runs)
+        return {
+            "impl": "reference", "metric": OP_METRIC[args.op], "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(r[2] for r in runs) / len(runs),
+            "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "each step: " + runs[-1][1]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     lens = np.diff(p.rowptr.astype(np.int64))
     total_fma = float(lens.sum()) * p.N
     if total_fma <= 4e8:
@@ -251,29 +313,53 @@ def gpu_arm(args, p, cfg, ws, rank, local):
     import torch
     from csr_spmm_02_gb300 import spmm
 
+    op = args.op
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-    bf16 = p.b_dtype == "bf16"
-    B_host = p.B.view(np.int16) if bf16 else p.B
+    bf16 = op == "spmm" and p.b_dtype == "bf16"
     rowptr = torch.from_numpy(p.rowptr).to(dev)
     colind = torch.from_numpy(p.colind).to(dev)
-    vals = torch.from_numpy(p.vals).to(dev)
-    B = torch.from_numpy(np.ascontiguousarray(B_host)).to(dev)
-    C = torch.empty((p.M, p.N), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    # host copies of the inputs (pinned later for the end-to-end leg) and the output shape
+    if op == "spmm":
+        host = {"colind": p.colind, "vals": p.vals,
+                "B": np.ascontiguousarray(p.B.view(np.int16) if bf16 else p.B)}
+        out_shape = (p.M, p.N)
+    else:
+        Ch, Bh, Dh = op_dense_inputs(p, op)
+        host = {"colind": p.colind, "C": Ch, "B": Bh}
+        if op == "fusedmm":
+            host["D"] = Dh
+        out_shape = (p.nnz,) if op == "sddmm" else (p.M, p.N)
+    d = {k: torch.from_numpy(v).to(dev) for k, v in host.items()}
+    out = torch.empty(out_shape, dtype=torch.float32, device=dev)
 
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    plan = spmm.spmm_csr_plan(rowptr, p.M, p.nnz, p.N, kernel=args.kernel, items_per_cta=args.items_per_cta)
+    plan = spmm.spmm_csr_plan(rowptr, p.M, p.nnz, p.N, kernel=args.kernel if op == "spmm" else "auto",
+                              items_per_cta=args.items_per_cta)
     torch.cuda.synchronize()
     plan_ms = (time.perf_counter() - t0) * 1e3
     info = plan.info()
-    run = spmm.spmm_csr_bf16f32_exec if bf16 else spmm.spmm_csr_f32_exec
-    launches_per_step = 1 if info["kernel"] == "row" else 2
+    if op == "spmm":
+        run = spmm.spmm_csr_bf16f32_exec if bf16 else spmm.spmm_csr_f32_exec
+        kernel = info["kernel"]
+        launches_per_step = 1 if kernel == "row" else 2
 
-    def step():
-        run(plan, p.K, colind, vals, B, C)
+        def step(t=d):
+            run(plan, p.K, t["colind"], t["vals"], t["B"], out)
+    elif op == "sddmm":
+        kernel, launches_per_step = "sddmm", 1
+
+        def step(t=d):
+            spmm.spmm_csr_sddmm_f32(plan, p.K, t["colind"], t["C"], t["B"], out)
+    else:
+        kernel, launches_per_step = "fusedmm", 2
+
+        def step(t=d):
+            spmm.spmm_csr_fusedmm_f32(plan, p.K, t["colind"], t["C"], t["B"], t["D"], out)
+    split = launches_per_step > 1  # the plan records the split event after the dominant kernel
 
     for i in range(max(args.warmup, 0)):
         flush.fill_(float(i))
@@ -304,7 +390,8 @@ def gpu_arm(args, p, cfg, ws, rank, local):
         time.sleep(0.1)
     for i in range(steps):
         flush.fill_(float(i))
-        spmm.spmm_plan_set_split_event(plan, splits[i])
+        if split:
+            spmm.spmm_plan_set_split_event(plan, splits[i])
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -314,34 +401,48 @@ def gpu_arm(args, p, cfg, ws, rank, local):
     spmm.spmm_plan_set_split_event(plan, None)
     assert spmm.spmm_plan_check_device(plan) == 0, "device error word set"
 
+    flops = op_flops(p, op)
+    nbytes = op_bytes(p, op)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    main_ms = [s.elapsed_time(m) for s, m in zip(starts, splits)]
+    main_ms = [s.elapsed_time(m) for s, m in zip(starts, splits)] if split else step_ms
     local_sec = sum(step_ms) / 1e3
-    value_flops, slowest = whole_job_rate(float(p.flops()) * steps, local_sec)
+    value_flops, slowest = whole_job_rate(float(flops) * steps, local_sec)
     ms_per_step = slowest / steps * 1e3
     peak, peak_kind = measured_hbm_peak()
     mean_main = sum(main_ms) / len(main_ms)
-    achieved = p.compulsory_bytes() / (mean_main * 1e-3) / 1e9
-    traffic = ncu_traffic(p.name, info["kernel"])
-    eff_gbs = p.compulsory_bytes() / (ms_per_step * 1e-3) / 1e9 * 1.0
+    achieved = nbytes / (mean_main * 1e-3) / 1e9
+    traffic = ncu_traffic(p.name if op == "spmm" else f"{p.name}:{op}", kernel)
+    eff_gbs = nbytes / (ms_per_step * 1e-3) / 1e9
 
-    # end to end: pinned host inputs -> device, one-call API, C -> pinned host
+    # end to end: pinned host inputs -> device, the public call, result -> pinned host
     e2e = None
     if not args.no_e2e:
-        h = {"rowptr": torch.from_numpy(p.rowptr).pin_memory(), "colind": torch.from_numpy(p.colind).pin_memory(),
-             "vals": torch.from_numpy(p.vals).pin_memory(),
-             "B": torch.from_numpy(np.ascontiguousarray(B_host)).pin_memory()}
-        d = {"rowptr": rowptr, "colind": colind, "vals": vals, "B": B}
-        C_host = torch.empty((p.M, p.N), dtype=torch.float32).pin_memory()
-        one_call = spmm.spmm_csr_bf16f32 if bf16 else spmm.spmm_csr_f32
+        h = {k: torch.from_numpy(v).pin_memory() for k, v in host.items()}
+        out_host = torch.empty(out_shape, dtype=torch.float32).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in h.values())
-        d2h = C_host.numel() * 4
+        d2h = out_host.numel() * 4
+        if op == "spmm":
+            h["rowptr"] = torch.from_numpy(p.rowptr).pin_memory()
+            h2d += h["rowptr"].numel() * 4
+            e2e_dev = dict(d, rowptr=rowptr)
+            one_call = spmm.spmm_csr_bf16f32 if bf16 else spmm.spmm_csr_f32
+            api = "spmm_csr_bf16f32" if bf16 else "spmm_csr_f32"
+
+            def call():
+                one_call(p.M, p.K, p.N, e2e_dev["rowptr"], e2e_dev["colind"], e2e_dev["vals"], e2e_dev["B"], out)
+        else:
+            e2e_dev = d
+            api = (f"spmm_csr_{op}_f32 on a plan built once for the fixed pattern "
+                   "(rowptr is not re-sent; colind and the dense operands are)")
+
+            def call():
+                step(e2e_dev)
 
         def e2e_step():
             for k in h:
-                d[k].copy_(h[k], non_blocking=True)
-            one_call(p.M, p.K, p.N, d["rowptr"], d["colind"], d["vals"], d["B"], C)
-            C_host.copy_(C, non_blocking=True)
+                e2e_dev[k].copy_(h[k], non_blocking=True)
+            call()
+            out_host.copy_(out, non_blocking=True)
             torch.cuda.current_stream().synchronize()
 
         for _ in range(2):
@@ -352,30 +453,33 @@ def gpu_arm(args, p, cfg, ws, rank, local):
         for _ in range(n_e2e):
             e2e_step()
         e2e_sec = time.perf_counter() - t0
-        e2e_rate, _ = whole_job_rate(float(p.flops()) * n_e2e, e2e_sec)
+        e2e_rate, _ = whole_job_rate(float(flops) * n_e2e, e2e_sec)
         e2e = {"value": e2e_rate / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": n_e2e, "api": "spmm_csr_bf16f32" if bf16 else "spmm_csr_f32"}
+               "steps": n_e2e, "api": api}
 
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
-        val, desc = time_oracle(p, args.cpu_seconds)
+        val, desc, _ = time_oracle(p, args.cpu_seconds, op, None if op == "spmm" else (Ch, Bh, Dh))
         cpu = {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
 
     cfg = dict(cfg)
-    cfg.update({"kernel": info["kernel"], "items_per_cta": info["items_per_cta"], "num_ctas": info["num_ctas"],
+    cfg.update({"op": op, "kernel": kernel, "items_per_cta": info["items_per_cta"], "num_ctas": info["num_ctas"],
                 "plan_ms": round(plan_ms, 3), "max_row_nnz": info["max_row_nnz"],
                 "l2": f"flushed before every timed step (write of {FLUSH_BYTES >> 20} MiB)",
                 "timing": "CUDA events per step on the launch stream; plan built once before timing"})
+    if op != "spmm":
+        cfg["b_dtype"] = "f32"
+        cfg["compulsory_bytes"] = nbytes
+        cfg["dense_operands"] = "C, D seeded uniform(-1, 1) fp32; B the workload's B in fp32"
     line = {
-        "metric": METRIC, "value": value_flops / 1e9, "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "metric": OP_METRIC[op], "value": value_flops / 1e9, "unit": UNIT, "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy PCG64)", "config": cfg,
         "effective_hbm_gbs": eff_gbs, "effective_hbm_frac": eff_gbs / peak,
-        "gflops_best": p.flops() / (min(step_ms) * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": info["kernel"], "achieved": achieved, "peak": peak,
+        "gflops_best": flops / (min(step_ms) * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "algorithmic_bytes": p.compulsory_bytes(),
-                     "kernel_ms": mean_main},
+                     "traffic": traffic, "algorithmic_bytes": nbytes, "kernel_ms": mean_main},
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": steps * launches_per_step,
     }
     plan.destroy()
@@ -391,6 +495,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=gen.WORKLOAD_ORDER, default="uniform64k")
+    ap.add_argument("--op", choices=["spmm", "sddmm", "fusedmm"], default="spmm")
     ap.add_argument("--kernel", choices=["auto", "row", "balanced"], default="auto")
     ap.add_argument("--items-per-cta", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -402,8 +507,8 @@ def main(argv=None):
     if args.impl == "reference" and rank != 0:
         return 0  # rank 0 alone times the CPU oracle
     p = gen.make_workload(args.workload)
-    cfg = {"workload": args.workload, "M": p.M, "K": p.K, "N": p.N, "nnz": p.nnz, "b_dtype": p.b_dtype,
-           "seed": p.seed, "compulsory_bytes": p.compulsory_bytes()}
+    cfg = {"workload": args.workload if args.op == "spmm" else f"{args.workload} pattern, {args.op}", "M": p.M, "K": p.K, "N": p.N, "nnz": p.nnz, "b_dtype": p.b_dtype,
+           "seed": p.seed, "compulsory_bytes": op_bytes(p, args.op)}
     if args.impl == "reference":
         print(json.dumps(reference_arm(args, p, cfg)), flush=True)
         return 0

@@ -52,6 +52,9 @@
 #ifndef SPMM_BAL_LOADS
 #define SPMM_BAL_LOADS 8  // 16-byte B loads in flight per lane (U steps x NCH chunks)
 #endif
+#ifndef SPMM_FUSED_LOADS
+#define SPMM_FUSED_LOADS 4  // FusedMM: steps per batch (three 16-byte operand slices each)
+#endif
 #ifndef SPMM_BAL_MIN_BLOCKS
 #define SPMM_BAL_MIN_BLOCKS 4  // resident CTAs asked of the compiler (fp32, one chunk per lane)
 #endif
@@ -62,16 +65,18 @@ namespace spmm {
 constexpr int kSlotHead = 1;    // the row began before the warp and ends in it
 constexpr int kSlotMiddle = 2;  // the warp lies entirely inside the row
 
-template <int NCH>
+template <int NCH, bool FUSED = false>
 struct BalancedSteps {
-  static constexpr int value = SPMM_BAL_LOADS / NCH > 0 ? SPMM_BAL_LOADS / NCH : 1;
+  static constexpr int kLoads = FUSED ? SPMM_FUSED_LOADS : SPMM_BAL_LOADS;
+  static constexpr int value = kLoads / NCH > 0 ? kLoads / NCH : 1;
 };
 
-// The 64-register budget of 4 resident CTAs fits the fp32 one-chunk shapes
-// without spills; wider or bf16 lanes keep the compiler's own choice.
-template <typename BT, int NCH>
+// The 64-register budget of 4 resident CTAs fits the fp32 one-chunk SpMM
+// shapes without spills; FusedMM (two gathered operands per nonzero plus the
+// C slices) gets 128 registers; wider or bf16 lanes keep the compiler's choice.
+template <typename BT, int NCH, bool FUSED>
 struct BalancedMinBlocks {
-  static constexpr int value = (sizeof(BT) == 4 && NCH == 1) ? SPMM_BAL_MIN_BLOCKS : 1;
+  static constexpr int value = FUSED ? 2 : (sizeof(BT) == 4 && NCH == 1) ? SPMM_BAL_MIN_BLOCKS : 1;
 };
 
 __host__ __device__ constexpr size_t balanced_smem_layout_bytes(int W, int TW, int T) {
@@ -82,19 +87,20 @@ __host__ __device__ constexpr size_t balanced_smem_layout_bytes(int W, int TW, i
 }
 
 template <typename BT, int VEC, int G, int NCH, bool FUSED>
-__global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
+__global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::value)
     spmm_balanced_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr,
                          const int32_t* __restrict__ colind, const float* __restrict__ vals,
                          const BT* __restrict__ B, float* __restrict__ C,
                          const int2* __restrict__ part, int32_t T, float* __restrict__ carry,
                          int* __restrict__ err, const float* __restrict__ Cd, const float* __restrict__ Bd) {
-  // FUSED: B is D (gathered and accumulated), Cd and Bd the SDDMM operands, vals unused.
+  // FUSED: B is D (gathered and accumulated), Cd and Bd the SDDMM operands, vals
+  // unused (its staging area holds the local row of every staged nonzero).
   static_assert(!FUSED || sizeof(BT) == 4, "FusedMM is fp32");
   using DotSlice = BSlice<float, FUSED ? VEC : 1>;  // fp32 slices of the dot-product operands
   constexpr int S = 32 / G;                // nonzeros per warp step
   constexpr int W = kThreads / 32;         // warps (workers) per CTA
   constexpr int TW = G * VEC * NCH;        // columns per tile
-  constexpr int U = BalancedSteps<NCH>::value;  // steps per batch
+  constexpr int U = BalancedSteps<NCH, FUSED>::value;  // steps per batch
 
   extern __shared__ __align__(16) unsigned char smem[];
   const int Tpad = T + 8;
@@ -165,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
   const int grp = lane / G;       // which nonzero of a step this lane's group takes
   const int gl = lane & (G - 1);  // lane within its group
   const int* rp = s_rp + (i0 - rbase);  // rp[r] = rowptr[i0 + r], 0 <= r <= i1 - i0
+  int* const s_row = reinterpret_cast<int*>(s_val);
+  if constexpr (FUSED) fill_row_ids(rp, i1 - i0, p0, p1, nbase, s_row);
   const int items = (i1 - i0) + (p1 - p0);
   const int Tw = T / W;
   auto find_row = [&](int dl) {  // first local row whose end lies at or after diagonal dl
@@ -190,49 +198,63 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
   }
   const int* colw = s_col - nbase + grp;  // colw[a] = colind of nonzero a + grp (staged)
   const float* valw = s_val - nbase + grp;
-  // FusedMM: dot-product operands of this lane (first column tile of C and Bd),
-  // the row of the group's current nonzero, and that row's C slice.
+  // FusedMM: this lane's columns of the dot-product operands (first tile).
   int dcoff[NCH];
   bool dvalid[NCH];
-  const float* bdl[NCH];
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
     const int col = (ch * G + gl) * VEC;
     dvalid[ch] = col < N;
     dcoff[ch] = min(col, N - VEC);
-    bdl[ch] = FUSED ? Bd + dcoff[ch] : nullptr;
   }
-  const int last_row = i1 - i0;
-  int rg = rw0, loaded = -1;
-  FVec<VEC> cfr[FUSED ? NCH : 1];
-  // Group sums of the dot products of the U steps starting at q (all lanes take part).
-  auto fused_values = [&](int q, const DotSlice (&bd)[FUSED ? BalancedSteps<NCH>::value : 1][NCH],
-                          float (&v)[FUSED ? BalancedSteps<NCH>::value : 1]) {
+  const float* const Crow0 = FUSED ? Cd + size_t(i0) * N : nullptr;
+  // Issue the loads of both dot-product operand slices of the nonzero staged at index k.
+  auto load_dot = [&](int k, DotSlice (&bd)[NCH], DotSlice (&cd)[NCH]) {
     if constexpr (FUSED) {
+      const size_t boff = size_t(s_col[k]) * N;
+      const size_t coff = size_t(s_row[k]) * N;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        bd[ch].load(Bd + boff + dcoff[ch]);
+        cd[ch].load(Crow0 + coff + dcoff[ch]);
+      }
+    }
+  };
+  // Values of the U steps starting at q: each lane's partial dot products,
+  // summed over its group by the transposed butterfly, then handed to the
+  // group's lanes one step at a time (all lanes take part).
+  auto fused_values = [&](int q, const DotSlice (&bd)[FUSED ? U : 1][NCH], const DotSlice (&cd)[FUSED ? U : 1][NCH],
+                          float (&v)[FUSED ? U : 1]) {
+    if constexpr (FUSED) {
+      constexpr int P = U < G ? U : G;  // values a lane ends with: steps gl % P of each round of P
+      float d[U];
 #pragma unroll
       for (int s = 0; s < U; ++s) {
-        const int n = q + s * S + grp;
-        float d = 0.f;
-        if (n < pw1) {
-          while (rg < last_row && rp[rg + 1] <= n) ++rg;
-          if (rg != loaded) {
-            const float* crow = Cd + size_t(i0 + rg) * N;
+        FVec<VEC> b[NCH], c[NCH];
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-              DotSlice t;
-              t.load(crow + dcoff[ch]);
-              t.widen(cfr[ch]);
-            }
-            loaded = rg;
-          }
-          FVec<VEC> b[NCH];
-#pragma unroll
-          for (int ch = 0; ch < NCH; ++ch) bd[s][ch].widen(b[ch]);
-          d = dot_lane<VEC, NCH>(cfr, b, dvalid, 0.f);
-          if (N > G * VEC * NCH)
-            d = dot_tail_tiles<VEC, G, NCH>(Cd + size_t(i0 + rg) * N, Bd + size_t(colw[q + s * S]) * N, N, gl, d);
+        for (int ch = 0; ch < NCH; ++ch) {
+          bd[s][ch].widen(b[ch]);
+          cd[s][ch].widen(c[ch]);
         }
-        v[s] = group_sum<G>(d);
+        d[s] = dot_lane<VEC, NCH>(c, b, dvalid);
+        if (N > G * VEC * NCH) {
+          const int k = min(q + s * S + grp, pw1 - 1) - nbase;
+          d[s] += dot_tail_tiles<VEC, G, NCH>(Crow0 + size_t(s_row[k]) * N, Bd + size_t(s_col[k]) * N, N, gl);
+        }
+      }
+      if constexpr (G == 1) {
+#pragma unroll
+        for (int s = 0; s < U; ++s) v[s] = d[s];
+      } else {
+#pragma unroll
+        for (int r0 = 0; r0 < U; r0 += P) {
+          float t[P];
+#pragma unroll
+          for (int i = 0; i < P; ++i) t[i] = d[r0 + i];
+          const float x = group_reduce_transposed<G, P>(t, gl);
+#pragma unroll
+          for (int i = 0; i < P; ++i) v[r0 + i] = __shfl_sync(0xffffffffu, x, grp * G + i);
+        }
       }
     }
   };
@@ -303,18 +325,16 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
   int q = pw0;
   for (; q + U * S <= pw1; q += U * S) {  // full batches
     BSlice<BT, VEC> bs[U][NCH];
-    DotSlice bd[FUSED ? U : 1][NCH];
+    DotSlice bd[FUSED ? U : 1][NCH], cd[FUSED ? U : 1][NCH];
     float fv[FUSED ? U : 1];
 #pragma unroll
     for (int s = 0; s < U; ++s) {  // gathers first
       const size_t roff = size_t(colw[q + s * S]) * N;
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        bs[s][ch].load(bl[ch] + roff);
-        if constexpr (FUSED) bd[s][ch].load(bdl[ch] + roff);
-      }
+      for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
+      if constexpr (FUSED) load_dot(q + s * S + grp - nbase, bd[s], cd[s]);
     }
-    fused_values(q, bd, fv);
+    fused_values(q, bd, cd, fv);
     auto value = [&](int s) {
       if constexpr (FUSED) return fv[s]; else return valw[q + s * S];
     };
@@ -336,24 +356,22 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH>::value)
   }
   if (q < pw1) {  // short last batch: slots past the sub-range re-read its last nonzero's row, value 0
     BSlice<BT, VEC> bs[U][NCH];
-    DotSlice bd[FUSED ? U : 1][NCH];
+    DotSlice bd[FUSED ? U : 1][NCH], cd[FUSED ? U : 1][NCH];
     float fv[FUSED ? U : 1];
 #pragma unroll
     for (int s = 0; s < U; ++s) {
       const size_t roff = size_t(colw[min(q + s * S, pw1 - 1 - grp)]) * N;
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        bs[s][ch].load(bl[ch] + roff);
-        if constexpr (FUSED) bd[s][ch].load(bdl[ch] + roff);
-      }
+      for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
+      if constexpr (FUSED) load_dot(min(q + s * S + grp, pw1 - 1) - nbase, bd[s], cd[s]);
     }
-    fused_values(q, bd, fv);
+    fused_values(q, bd, cd, fv);
 #pragma unroll
     for (int s = 0; s < U; ++s) {
       const int a = q + s * S;
       if (a >= pw1) break;
       float v;
-      if constexpr (FUSED) v = fv[s]; else v = a + grp < pw1 ? valw[a] : 0.f;
+      if constexpr (FUSED) v = a + grp < pw1 ? fv[s] : 0.f; else v = a + grp < pw1 ? valw[a] : 0.f;
       step(a, v, bs[s]);
     }
   }

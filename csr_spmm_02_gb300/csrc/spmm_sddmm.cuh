@@ -4,13 +4,24 @@
 // Matrix Kernels on Intel Max Series GPU" (Algorithm 1, Figs. 3-4, 7) assigns
 // each row of the sparse output to one or more work-items (NT per row), keeps
 // the row C_i in registers and produces every nonzero of the row as a dot
-// product with the row B_j it selects.  Here the rows of a CTA come from the
-// same merge-path ranges as the SpMM kernels (balanced in rows + nonzeros), a
-// warp takes a sub-range, and its S = 32/G lane groups take consecutive
-// nonzeros: a group keeps the C row of its current nonzero's row in registers
-// (reloaded when the row changes), gathers the B row with 16-byte loads, and
-// its G lanes add their partial dot products with shuffles before one lane
-// stores the value.  Each output is written once; no reduction crosses CTAs.
+// product with the row B_j it selects.  Here the nonzeros of a CTA come from
+// the same merge-path ranges as the SpMM kernels, and the work is laid out for
+// a warp rather than for a row:
+//
+//  * the CTA stages its colind and rowptr slices in shared memory and writes
+//    the (local) row of every staged nonzero next to its column, so a lane
+//    finds both rows of a dot product with two shared loads, without a walk;
+//  * a warp takes rounds of 32 consecutive nonzeros; its S = 32/G lane groups
+//    take every S-th one, each lane holding VEC*NCH columns of both operands
+//    (16-byte loads; the C row is re-read per nonzero and is an L1 hit while
+//    the row lasts, so no load waits on a row change);
+//  * a lane keeps the partial dot products of G nonzeros and the group sums
+//    them with a transposed butterfly: G-1 shuffles for G results instead of
+//    log2(G) per result, after which lane l of the group holds nonzero l's
+//    value and the warp stores its 32 values with one coalesced store.
+//
+// Each output is written once; no reduction crosses lanes of different
+// nonzeros or CTAs, and the summation order is fixed (deterministic).
 #pragma once
 
 #include <climits>
@@ -18,39 +29,60 @@
 #include "spmm_device.cuh"
 #include "spmm_internal.h"
 
+#ifndef SPMM_SDDMM_LOADS
+#define SPMM_SDDMM_LOADS 4  // nonzeros whose operand rows a lane has in flight (per chunk)
+#endif
+
 namespace spmm {
 
 __host__ __device__ constexpr size_t sddmm_smem_layout_bytes(int T) {
-  return size_t(2) * (T + 8) * 4 + 16;  // colind and rowptr slices, mbarrier
+  return size_t(3) * (T + 8) * 4 + 16;  // colind, row ids, rowptr slices; mbarrier
 }
 
-// A lane's share of a dot product: chunks whose columns lie past N (their
-// loads were clamped into the row) contribute nothing.
+// Local row of every staged nonzero n in [p0, p1): the largest r <= last_row
+// with rp[r] <= n (rows with no nonzeros are skipped by that rule).  Ends with
+// a CTA barrier.
+__device__ __forceinline__ void fill_row_ids(const int* rp, int last_row, int p0, int p1, int nbase, int* s_row) {
+  for (int n = p0 + int(threadIdx.x); n < p1; n += kThreads) {
+    int lo = 0, hi = last_row;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (rp[mid] <= n) lo = mid; else hi = mid - 1;
+    }
+    s_row[n - nbase] = lo;
+  }
+  __syncthreads();
+}
+
+// A lane's share of one dot product over its NCH chunks; chunks whose columns
+// lie past N (their loads were clamped into the row) contribute nothing.
 template <int VEC, int NCH>
 __device__ __forceinline__ float dot_lane(const FVec<VEC> (&c)[NCH], const FVec<VEC> (&b)[NCH],
-                                          const bool (&valid)[NCH], float d) {
+                                          const bool (&valid)[NCH]) {
+  if constexpr (VEC == 1) {
+    float d = 0.f;
 #pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) {
-    float t = 0.f;
-    if constexpr (VEC == 1) {
-      t = c[ch].x * b[ch].x;
-    } else {
+    for (int ch = 0; ch < NCH; ++ch) d = valid[ch] ? fmaf(c[ch].x, b[ch].x, d) : d;
+    return d;
+  } else {
+    float2 t = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < VEC / 2; ++j) {
-        t = fmaf(c[ch].p[j].x, b[ch].p[j].x, t);
-        t = fmaf(c[ch].p[j].y, b[ch].p[j].y, t);
-      }
+    for (int ch = 0; ch < NCH; ++ch) {
+      float2 u = __fmul2_rn(c[ch].p[0], b[ch].p[0]);
+#pragma unroll
+      for (int j = 1; j < VEC / 2; ++j) u = __ffma2_rn(c[ch].p[j], b[ch].p[j], u);
+      t = valid[ch] ? __fadd2_rn(t, u) : t;
     }
-    d += valid[ch] ? t : 0.f;
+    return t.x + t.y;
   }
-  return d;
 }
 
-// Dot-product share of a lane over the column tiles after the first
-// (rows wider than one tile of G*VEC*NCH columns); loads are not batched.
+// Dot-product share of a lane over the column tiles after the first (rows
+// wider than one tile of G*VEC*NCH columns); loads are not batched.
 template <int VEC, int G, int NCH>
-__device__ __forceinline__ float dot_tail_tiles(const float* crow, const float* brow, int N, int gl, float d) {
+__device__ __forceinline__ float dot_tail_tiles(const float* crow, const float* brow, int N, int gl) {
   constexpr int TW = G * VEC * NCH;
+  float d = 0.f;
   for (int t0 = TW; t0 < N; t0 += TW) {
     FVec<VEC> c[NCH], b[NCH];
     bool valid[NCH];
@@ -65,17 +97,34 @@ __device__ __forceinline__ float dot_tail_tiles(const float* crow, const float* 
       x.widen(c[ch]);
       y.widen(b[ch]);
     }
-    d = dot_lane<VEC, NCH>(c, b, valid, d);
+    d += dot_lane<VEC, NCH>(c, b, valid);
   }
   return d;
 }
 
-// Sum over the G lanes of each group (every lane of the warp takes part).
-template <int G>
-__device__ __forceinline__ float group_sum(float d) {
+// Group sums of P partial values per lane (P <= G, both powers of two): on
+// return every lane gl holds the sum over its G-lane group of v[gl % P].
+// Offsets >= P are plain butterfly levels on all P values; the last log2(P)
+// levels are transposed: a lane sends the half of its values that its partner
+// keeps, so they cost P-1 shuffles in all.  Every lane of the warp takes part.
+template <int G, int P>
+__device__ __forceinline__ float group_reduce_transposed(float (&v)[P], int gl) {
+  static_assert(P <= G && (P & (P - 1)) == 0 && (G & (G - 1)) == 0, "powers of two, P <= G");
 #pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-  return d;
+  for (int o = G / 2; o >= P; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < P; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+#pragma unroll
+  for (int o = P / 2; o >= 1; o >>= 1) {
+    const bool upper = (gl & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
 }
 
 template <int VEC, int G, int NCH>
@@ -83,15 +132,19 @@ __global__ void __launch_bounds__(kThreads)
     spmm_sddmm_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr, const int32_t* __restrict__ colind,
                       const float* __restrict__ Cd, const float* __restrict__ B, float* __restrict__ out,
                       const int2* __restrict__ part, int32_t T, int* __restrict__ err) {
-  constexpr int S = 32 / G;
+  constexpr int S = 32 / G;                     // nonzeros per warp step
   constexpr int W = kThreads / 32;
-  constexpr int U = 8 / NCH > 0 ? 8 / NCH : 1;  // steps per batch
+  constexpr int U = SPMM_SDDMM_LOADS / NCH > 0 ? SPMM_SDDMM_LOADS / NCH : 1;  // steps per load batch
+  constexpr int R = G > U ? G : U;              // steps per warp iteration
+  constexpr int NPI = R * S;                    // nonzeros per warp iteration
+  static_assert(R % U == 0 && R % G == 0, "powers of two");
 
   extern __shared__ __align__(16) unsigned char smem[];
   const int Tpad = T + 8;
   int* s_col = reinterpret_cast<int*>(smem);
-  int* s_rp = s_col + Tpad;
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_col + 2 * Tpad);
+  int* s_row = s_col + Tpad;
+  int* s_rp = s_col + 2 * Tpad;
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_col + 3 * Tpad);
 
   const int tid = threadIdx.x;
   const int2 beg = __ldg(part + blockIdx.x);
@@ -132,75 +185,59 @@ __global__ void __launch_bounds__(kThreads)
     mbar_wait_bounded(bar, 0, kSpinLimit);
     return;
   }
+  fill_row_ids(s_rp + (i0 - rbase), i1 - i0, p0, p1, nbase, s_row);
 
-  // ---- this warp's sub-range --------------------------------------------------
+  // ---- rounds of nonzeros ---------------------------------------------------
   const int w = tid >> 5, lane = tid & 31, grp = lane / G, gl = lane & (G - 1);
-  const int* rp = s_rp + (i0 - rbase);
-  const int items = (i1 - i0) + (p1 - p0);
-  const int Tw = T / W;
-  auto find_row = [&](int dl) {
-    int lo = 0, hi = i1 - i0;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (rp[mid + 1] - p0 + mid >= dl) hi = mid; else lo = mid + 1;
-    }
-    return lo;
-  };
-  const int dl0 = min(w * Tw, items), dl1 = min(dl0 + Tw, items);
-  const int rw0 = find_row(dl0), rw1 = find_row(dl1);
-  const int pw0 = p0 + dl0 - rw0, pw1 = p0 + dl1 - rw1;
-  if (pw0 >= pw1) return;  // no nonzeros in this sub-range (uniform in the warp)
-
   int coffl[NCH];
   bool valid[NCH];
-  const float* bl[NCH];
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
     const int col = (ch * G + gl) * VEC;  // first column tile
     valid[ch] = col < N;
     coffl[ch] = min(col, N - VEC);
-    bl[ch] = B + coffl[ch];
   }
-  const int last_row = i1 - i0;  // rows past it hold no nonzero of this CTA
-  const int* colw = s_col - nbase + grp;
-  int rg = rw0;      // row of this group's current nonzero (local)
-  int loaded = -1;   // row whose C slice is in c
-  FVec<VEC> c[NCH];
-  for (int q = pw0; q < pw1; q += U * S) {
-    BSlice<float, VEC> bs[U][NCH];
+  const float* Crow0 = Cd + size_t(i0) * N;
+  for (int base = p0 + w * NPI; base < p1; base += W * NPI) {
+    float dots[R];
 #pragma unroll
-    for (int s = 0; s < U; ++s) {
-      const size_t roff = size_t(colw[min(q + s * S, pw1 - 1 - grp)]) * N;
+    for (int s0 = 0; s0 < R; s0 += U) {
+      BSlice<float, VEC> bs[U][NCH], cs[U][NCH];
+      int ks[U];
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
+      for (int u = 0; u < U; ++u) {  // gathers first: both operand rows of U nonzeros
+        const int k = min(base + (s0 + u) * S + grp, p1 - 1) - nbase;
+        ks[u] = k;
+        const size_t boff = size_t(s_col[k]) * N;
+        const size_t coff = size_t(s_row[k]) * N;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          bs[u][ch].load(B + boff + coffl[ch]);
+          cs[u][ch].load(Crow0 + coff + coffl[ch]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        FVec<VEC> b[NCH], c[NCH];
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          bs[u][ch].widen(b[ch]);
+          cs[u][ch].widen(c[ch]);
+        }
+        float d = dot_lane<VEC, NCH>(c, b, valid);
+        if (N > G * VEC * NCH)
+          d += dot_tail_tiles<VEC, G, NCH>(Crow0 + size_t(s_row[ks[u]]) * N, B + size_t(s_col[ks[u]]) * N, N, gl);
+        dots[s0 + u] = d;
+      }
     }
 #pragma unroll
-    for (int s = 0; s < U; ++s) {
-      const int a = q + s * S;
-      if (a >= pw1) break;
-      const int n = a + grp;
-      float d = 0.f;
-      if (n < pw1) {
-        while (rg < last_row && rp[rg + 1] <= n) ++rg;  // rows only advance along the sub-range
-        if (rg != loaded) {
-          const float* crow = Cd + size_t(i0 + rg) * N;
+    for (int r0 = 0; r0 < R; r0 += G) {  // one round: G steps, S*G = 32 nonzeros
+      float v[G];
 #pragma unroll
-          for (int ch = 0; ch < NCH; ++ch) {
-            BSlice<float, VEC> t;
-            t.load(crow + coffl[ch]);
-            t.widen(c[ch]);
-          }
-          loaded = rg;
-        }
-        FVec<VEC> b[NCH];
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) bs[s][ch].widen(b[ch]);
-        d = dot_lane<VEC, NCH>(c, b, valid, 0.f);
-        if (N > G * VEC * NCH)
-          d = dot_tail_tiles<VEC, G, NCH>(Cd + size_t(i0 + rg) * N, B + size_t(colw[a]) * N, N, gl, d);
-      }
-      d = group_sum<G>(d);
-      if (gl == 0 && n < pw1) st_stream1(out + n, d);
+      for (int i = 0; i < G; ++i) v[i] = dots[r0 + i];
+      const float x = group_reduce_transposed<G, G>(v, gl);
+      const int n = base + (r0 + gl) * S + grp;  // the warp's 32 lanes cover 32 consecutive nonzeros
+      if (n < p1) st_stream1(out + n, x);
     }
   }
 }

@@ -109,6 +109,11 @@ def _draw_f32(rng: np.random.Generator, n: int, dist: str) -> np.ndarray:
     return out
 
 
+def dense_f32(rng: np.random.Generator, rows: int, cols: int, dist: str = "pm1") -> np.ndarray:
+    """A seeded row-major fp32 matrix (the dense operands of SDDMM / FusedMM)."""
+    return _draw_f32(rng, rows * cols, dist).reshape(rows, cols)
+
+
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 values to bf16 (nearest, ties to even); return uint16 bits.
 
