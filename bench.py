@@ -345,7 +345,7 @@ def gpu_arm(args, p, cfg, ws, rank, local):
     if op == "spmm":
         run = spmm.spmm_csr_bf16f32_exec if bf16 else spmm.spmm_csr_f32_exec
         kernel = info["kernel"]
-        launches_per_step = 1 if kernel == "row" else 2
+        launches_per_step = 2 if kernel == "balanced" else 1
 
         def step(t=d):
             run(plan, p.K, t["colind"], t["vals"], t["B"], out)
@@ -496,7 +496,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=gen.WORKLOAD_ORDER, default="uniform64k")
     ap.add_argument("--op", choices=["spmm", "sddmm", "fusedmm"], default="spmm")
-    ap.add_argument("--kernel", choices=["auto", "row", "balanced"], default="auto")
+    ap.add_argument("--kernel", choices=["auto", "row", "balanced", "window"], default="auto")
     ap.add_argument("--items-per-cta", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -60,8 +60,9 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
   if (!guard.ok) return SPMM_ERR_CUDA;
 
   const bool vector_ok = plan->N % (bf16 ? 8 : 4) == 0 && aligned16(B) && aligned16(C);
-  const Shape s = plan->kernel == SPMM_KERNEL_ROW ? choose_shape(plan->N, bf16, vector_ok)
-                                                  : choose_shape_balanced(plan->N, bf16, vector_ok);
+  const bool row_family = plan->kernel == SPMM_KERNEL_ROW || plan->kernel == SPMM_KERNEL_WINDOW;
+  const Shape s = row_family ? choose_shape(plan->N, bf16, vector_ok) : choose_shape_balanced(plan->N, bf16, vector_ok);
+  const bool window = plan->kernel == SPMM_KERNEL_WINDOW && s.G == 32 && s.nch == 1 && s.vec == (bf16 ? 8 : 4);
   Launch L{};
   L.M = plan->M;
   L.N = plan->N;
@@ -80,7 +81,10 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
   L.stream = stream;
 
   cudaError_t e;
-  if (plan->kernel == SPMM_KERNEL_ROW) {
+  if (window) {
+    e = bf16 ? launch_window_bf16(L) : launch_window_f32(L);
+    if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+  } else if (row_family) {
     e = bf16 ? launch_row_bf16(L, s) : launch_row_f32(L, s);
     if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
   } else {

@@ -122,6 +122,7 @@ template <>
 struct BSlice<float, 4> {
   float4 r;
   __device__ __forceinline__ void load(const float* p) { r = __ldg(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ void load_shared(const float* p) { r = *reinterpret_cast<const float4*>(p); }
   __device__ __forceinline__ void widen(FVec<4>& o) const {
     o.p[0] = make_float2(r.x, r.y);
     o.p[1] = make_float2(r.z, r.w);
@@ -143,6 +144,7 @@ template <>
 struct BSlice<uint16_t, 8> {
   uint4 r;
   __device__ __forceinline__ void load(const uint16_t* p) { r = __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ __forceinline__ void load_shared(const uint16_t* p) { r = *reinterpret_cast<const uint4*>(p); }
   __device__ __forceinline__ void widen(FVec<8>& o) const {
     o.p[0] = bf16x2_widen(r.x);
     o.p[1] = bf16x2_widen(r.y);

@@ -89,6 +89,8 @@ cudaError_t launch_row_f32(const Launch& L, Shape s);
 cudaError_t launch_row_bf16(const Launch& L, Shape s);
 cudaError_t launch_balanced_f32(const Launch& L, Shape s);
 cudaError_t launch_balanced_bf16(const Launch& L, Shape s);
+cudaError_t launch_window_f32(const Launch& L);
+cudaError_t launch_window_bf16(const Launch& L);
 cudaError_t launch_fixup(const Launch& L);
 cudaError_t launch_sddmm_f32(const Launch& L, Shape s, const float* Cd, float* out);
 cudaError_t launch_fusedmm_f32(const Launch& L, Shape s, const float* Cd, const float* Bd);

@@ -136,7 +136,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   if (M < 0 || N < 0 || nnz < 0) return SPMM_ERR_INVALID_ARG;
   if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
   if (M > 0 && !rowptr) return SPMM_ERR_INVALID_ARG;
-  if (kernel < SPMM_KERNEL_AUTO || kernel > SPMM_KERNEL_BALANCED) return SPMM_ERR_INVALID_ARG;
+  if (kernel < SPMM_KERNEL_AUTO || kernel > SPMM_KERNEL_WINDOW) return SPMM_ERR_INVALID_ARG;
   if (items_per_cta != 0 && (items_per_cta < 256 || items_per_cta > kMaxItemsPerCta || items_per_cta % 256 != 0))
     return SPMM_ERR_INVALID_ARG;
 
@@ -147,7 +147,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   plan->N = N;
   plan->rowptr = rowptr;
   plan->stream_ordered = stream_ordered;
-  plan->kernel = kernel == SPMM_KERNEL_BALANCED ? SPMM_KERNEL_BALANCED : SPMM_KERNEL_ROW;
+  plan->kernel = kernel == SPMM_KERNEL_AUTO ? SPMM_KERNEL_ROW : kernel;
   if (cudaGetDevice(&plan->device) != cudaSuccess) {
     delete plan;
     return SPMM_ERR_CUDA;
@@ -186,6 +186,9 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
     // merge-path split bounds every CTA's work.
     const double mean = double(nnz) / double(M);
     plan->kernel = double(plan->max_row_nnz) <= 4.0 * mean + 32.0 ? SPMM_KERNEL_ROW : SPMM_KERNEL_BALANCED;
+    // Rows wide enough for a warp per column tile: the window kernel (it
+    // falls back to per-row gathers where the columns are scattered).
+    if (plan->kernel == SPMM_KERNEL_ROW && N >= 128) plan->kernel = SPMM_KERNEL_WINDOW;
   }
 
   {  // merge-path partition and carry rows: used by the balanced SpMM, SDDMM and FusedMM

@@ -81,7 +81,16 @@ typedef enum {
 typedef enum {
   SPMM_KERNEL_AUTO = 0,      /* chosen from the row-length statistics */
   SPMM_KERNEL_ROW = 1,       /* one (sub-)warp group per row: short, uniform rows */
-  SPMM_KERNEL_BALANCED = 2   /* merge-path nnz-balanced split + fixup: skewed rows */
+  SPMM_KERNEL_BALANCED = 2,  /* merge-path nnz-balanced split + fixup: skewed rows */
+  SPMM_KERNEL_WINDOW = 3     /* short rows, B rows reused across rows: a CTA of 32 rows
+                              * whose columns span few enough B rows stages them in
+                              * shared memory and reuses each from registers for 4
+                              * rows; other CTAs gather as the row kernel.  Runs when a
+                              * warp covers the column tile (N >= 128 fp32 with 4-column
+                              * lanes, N >= 256 bf16 with 8-column lanes, 16-byte
+                              * aligned B and C); otherwise exec runs the row kernel.
+                              * Absent entries inside the window are multiplied as
+                              * zeros, so a NaN/Inf in such a B row reaches the row. */
 } spmm_kernel;
 
 /* Opaque plan: owns its device workspace (merge-path partition, carry rows
@@ -90,7 +99,7 @@ typedef struct spmm_plan_s* spmm_plan_t;
 
 /* What a plan decided (host copy, filled by spmm_plan_get_info). */
 typedef struct {
-  int32_t kernel;          /* SPMM_KERNEL_ROW or SPMM_KERNEL_BALANCED */
+  int32_t kernel;          /* SPMM_KERNEL_ROW, _BALANCED or _WINDOW */
   int32_t M;
   int64_t nnz;
   int32_t N;

@@ -44,8 +44,9 @@ def test_workload_parity(name):
     rows = sample_rows(p, rng)
     C_ref, S = H.reference(p, rows=rows)
     a = H.device_arrays(p)
-    expect_kernel = "row" if name in ("uniform1k", "uniform64k", "banded") else "balanced"
-    for kernel in ("auto", "balanced" if expect_kernel == "row" else "row"):
+    expect_kernel = {"uniform1k": "row", "uniform64k": "row", "banded": "window"}.get(name, "balanced")
+    others = {"row": ("balanced",), "window": ("row", "balanced"), "balanced": ("row",)}[expect_kernel]
+    for kernel in ("auto",) + others:
         C, plan = H.run(p, kernel=kernel, arrays=a)
         if kernel == "auto":
             assert plan.info()["kernel"] == expect_kernel

@@ -1,0 +1,117 @@
+"""The window kernel (B rows staged per CTA, reused across 4 rows per warp)
+vs the CPU oracle: both of its paths (window and gather), the boundary
+between them, duplicates and unsorted columns, CTAs too large to stage,
+empty CTAs, several column tiles, determinism."""
+import numpy as np
+import pytest
+import torch
+
+from csr_spmm_02_gb300 import gen
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+ROWS_PER_CTA = 32
+WINDOW_ROWS = 128  # B rows the shared-memory window holds for 512-byte tile rows
+
+
+def banded(seed, M, K, below, above, N, b_dtype="f32", integer=False, duplicates=False, unsorted=False,
+           empty_every=0, sparse_every=0, long_rows=(), ends_only=False):
+    """Row i holds columns max(0, i-below) .. min(K-1, i+above) (with ends_only,
+    only the two ends and the diagonal of that range), with options."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for i in range(M):
+        if (empty_every and i % empty_every == 3) or (sparse_every and i % sparse_every):
+            rows.append(np.zeros(0, np.int32))
+            continue
+        if i in dict(long_rows):
+            cols = np.sort(rng.choice(K, dict(long_rows)[i], replace=False)).astype(np.int32)
+        else:
+            cols = np.arange(max(0, i - below), min(K - 1, i + above) + 1, dtype=np.int32)
+            if ends_only:
+                cols = np.unique(np.array([cols[0], min(i, K - 1), cols[-1]], np.int32))
+        if duplicates and len(cols) and i % 5 == 0:
+            cols = np.concatenate([cols, cols[:2]])
+        if unsorted:
+            cols = rng.permutation(cols).astype(np.int32)
+        rows.append(cols)
+    rowptr = np.zeros(M + 1, np.int64)
+    rowptr[1:] = np.cumsum([len(r) for r in rows])
+    colind = np.concatenate(rows).astype(np.int32) if rowptr[-1] else np.zeros(0, np.int32)
+    nnz = int(rowptr[-1])
+    if integer:
+        vals = rng.integers(-2, 3, nnz).astype(np.float32)
+        Bf = rng.integers(-3, 4, (K, N)).astype(np.float32)
+    else:
+        vals = rng.standard_normal(nnz).astype(np.float32)
+        Bf = rng.standard_normal((K, N)).astype(np.float32)
+    B = Bf if b_dtype == "f32" else gen.f32_to_bf16_bits(Bf)
+    return gen.CsrProblem("banded-test", M, K, N, rowptr.astype(np.int32), colind, vals, B, b_dtype)
+
+
+def check(p, kernel="window"):
+    C, plan = H.run(p, kernel=kernel)
+    info = plan.info()
+    C_ref, S = H.reference(p)
+    H.assert_within(C, C_ref, S, p.b_dtype, f"{kernel}/{p.b_dtype}/N={p.N}")
+    plan.destroy()
+    return C, info
+
+
+@pytest.mark.parametrize("b_dtype,N", [("f32", 128), ("f32", 136), ("f32", 256), ("f32", 260),
+                                       ("bf16", 256), ("bf16", 264), ("bf16", 512)])
+def test_banded_parity(b_dtype, N):
+    p = banded(N, 1000, 1000, 32, 31, N, b_dtype=b_dtype)
+    _, info = check(p, kernel="auto")
+    assert info["kernel"] == "window"
+
+
+@pytest.mark.parametrize("width", [95, 96, 97])  # CTA spans of 127, 128 and 129 B rows
+def test_span_boundary(width):
+    below = width // 2
+    p = banded(width, 700, 800, below, width - below, 128, ends_only=True)
+    check(p)
+
+
+@pytest.mark.parametrize("b_dtype", ["f32", "bf16"])
+def test_integer_duplicates_unsorted_exact(b_dtype):
+    p = banded(7, 900, 950, 20, 25, 256, b_dtype=b_dtype, integer=True, duplicates=True, unsorted=True,
+               empty_every=7)
+    C, _ = H.run(p, kernel="window")
+    C_ref, _ = H.reference(p)
+    H.assert_exact(C, C_ref, f"window/{b_dtype}")
+
+
+def test_long_rows_use_the_gather_path():
+    # a CTA holding a 3000-nonzero row cannot stage; its neighbours still use the window
+    p = banded(8, 640, 4000, 10, 10, 128, long_rows=((40, 3000), (300, 1500), (601, 2100)))
+    check(p)
+
+
+def test_empty_ctas_and_ragged_tail():
+    p = banded(9, 32 * 9 + 7, 300, 3, 3, 256, b_dtype="bf16", sparse_every=100)  # CTAs 1, 2, 4, 5, 7 empty
+    C, _ = check(p)
+    rp = p.rowptr
+    empty = np.flatnonzero(np.diff(rp) == 0)
+    assert not bool(C[torch.from_numpy(empty).cuda()].any())
+    q = banded(10, 32 * 3 + 1, 64, 0, 0, 128)  # one diagonal, last CTA has one row
+    check(q)
+    z = gen.CsrProblem("empty", 70, 50, 128, np.zeros(71, np.int32), np.zeros(0, np.int32),
+                       np.zeros(0, np.float32), np.ones((50, 128), np.float32), "f32")
+    C, _ = H.run(z, kernel="window")
+    assert not bool(C.any())
+
+
+def test_scattered_columns_use_the_gather_path():
+    rng = np.random.default_rng(11)
+    for N, b in ((128, "f32"), (256, "bf16")):
+        p = gen.random_csr(rng, 1200, 5000, N, mean_row=12, empty_frac=0.2, long_rows=[(17, 2500)], b_dtype=b)
+        check(p)
+
+
+def test_deterministic():
+    p = banded(12, 2000, 2000, 32, 31, 256, b_dtype="bf16")
+    C1, _ = H.run(p, kernel="window")
+    C2, _ = H.run(p, kernel="window")
+    assert torch.equal(C1, C2)
