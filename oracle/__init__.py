@@ -16,6 +16,8 @@ Functions
 ``spmm_reference``     C and the magnitude sum S for all rows or a row list.
 ``sddmm_reference``    the sampled dot products out[p] = C_i . B_j and their bound.
 ``fusedmm_reference``  E = (SDDMM values) . D and its bound.
+``semiring_reference`` C with a general (+) / (x) pair (sum/min/max over
+                       multiply/add), and S for the sum.
 """
 from __future__ import annotations
 
@@ -62,6 +64,9 @@ def load_library(path: str) -> ctypes.CDLL:
     h = lib.fusedmm_oracle_f64
     h.restype = ctypes.c_int
     h.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    k = lib.spmm_semiring_oracle_f64
+    k.restype = ctypes.c_int
+    k.argtypes = [i32, i32, i32, vp, vp, vp, vp, i32, i32, vp, vp]
     return lib
 
 
@@ -160,3 +165,27 @@ def fusedmm_reference(rowptr, colind, C, B, D, *, library=None, with_values=Fals
     _check_rc(lib.fusedmm_oracle_f64(M, K, N, _ptr(rowptr), _ptr(colind), _ptr(C), _ptr(B), _ptr(D),
                                      _ptr(E), _ptr(S), _ptr(a)))
     return (E, S, a) if with_values else (E, S)
+
+
+SEMIRING_ADD = {"sum": 0, "min": 1, "max": 2}
+SEMIRING_MUL = {"mul": 0, "add": 1}
+
+
+def semiring_reference(rowptr, colind, vals, B, add="sum", mul="mul", *, library=None):
+    """(C, S): C[i, n] = add-reduction over row i of vals[p] mul B[colind[p], n], float64.
+
+    add in {"sum", "min", "max"}, mul in {"mul", "add"}; an empty row gives the
+    identity of add (0, +inf, -inf).  S (the magnitude sum) is filled for "sum"
+    and zero otherwise.  B is float32."""
+    rowptr = np.ascontiguousarray(rowptr, dtype=np.int32)
+    colind = np.ascontiguousarray(colind, dtype=np.int32)
+    vals = np.ascontiguousarray(vals, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    M = len(rowptr) - 1
+    K, N = B.shape
+    C = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64)
+    lib = library if library is not None else _lib()
+    _check_rc(lib.spmm_semiring_oracle_f64(M, K, N, _ptr(rowptr), _ptr(colind), _ptr(vals), _ptr(B),
+                                           SEMIRING_ADD[add], SEMIRING_MUL[mul], _ptr(C), _ptr(S)))
+    return C, S

@@ -156,3 +156,55 @@ int fusedmm_oracle_f64(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, c
   }
   return 0;
 }
+
+/*
+ * Semiring SpMM (page "Sgap: Towards Efficient Sparse Tensor Algebra
+ * Compilation for GPU", sparse-dense hybrid algebra section, Eq. 3): the
+ * reduction of SpMM generalised to a commutative operation (+) over the
+ * row's stored entries of a binary operation (x) of the entry's value and
+ * the dense element,
+ *
+ *     C[i][n] = (+)_{p = rowptr[i]}^{rowptr[i+1]-1} ( vals[p] (x) B[colind[p]][n] ).
+ *
+ * add_op: 0 = sum, 1 = min, 2 = max.  mul_op: 0 = multiply, 1 = add.  An
+ * empty row gives the identity of (+): 0, +infinity, -infinity.  Each (x) is
+ * one double-precision operation on two binary32 values (exact: a product of
+ * two 24-bit significands fits in 53 bits, and so does a sum whose exponents
+ * differ by at most 29; larger gaps round to the same binary32 either way).
+ * S_out (sum only, may be NULL) is sum_p |vals[p] (x) B[colind[p]][n]|.
+ * B is binary32.  Returns 0, -1 on an argument error, -2 on malformed CSR.
+ */
+int spmm_semiring_oracle_f64(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
+                             const int32_t* colind, const float* vals, const float* B,
+                             int32_t add_op, int32_t mul_op, double* C_out, double* S_out) {
+  if (M < 0 || K < 0 || N < 0 || !rowptr || !C_out) return -1;
+  if (add_op < 0 || add_op > 2 || mul_op < 0 || mul_op > 1) return -1;
+  const double identity = add_op == 0 ? 0.0 : (add_op == 1 ? INFINITY : -INFINITY);
+  for (int32_t i = 0; i < M; ++i) {
+    double* c = C_out + (int64_t)i * N;
+    double* s = S_out ? S_out + (int64_t)i * N : NULL;
+    for (int32_t n = 0; n < N; ++n) {
+      c[n] = identity;
+      if (s) s[n] = 0.0;
+    }
+    if (rowptr[i + 1] < rowptr[i]) return -2;
+    for (int64_t p = rowptr[i]; p < rowptr[i + 1]; ++p) {
+      const double a = (double)vals[p];
+      const int64_t j = colind[p];
+      if (j < 0 || j >= K) return -2;
+      for (int32_t n = 0; n < N; ++n) {
+        const double b = (double)B[j * N + n];
+        const double t = mul_op == 0 ? a * b : a + b;
+        if (add_op == 0) {
+          c[n] += t;
+          if (s) s[n] += fabs(t);
+        } else if (add_op == 1) {
+          if (t < c[n]) c[n] = t;
+        } else {
+          if (t > c[n]) c[n] = t;
+        }
+      }
+    }
+  }
+  return 0;
+}
