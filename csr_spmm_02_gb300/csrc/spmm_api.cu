@@ -60,7 +60,8 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
   if (!guard.ok) return SPMM_ERR_CUDA;
 
   const bool vector_ok = plan->N % (bf16 ? 8 : 4) == 0 && aligned16(B) && aligned16(C);
-  const bool row_family = plan->kernel == SPMM_KERNEL_ROW || plan->kernel == SPMM_KERNEL_WINDOW;
+  const bool row_family = plan->kernel == SPMM_KERNEL_ROW || plan->kernel == SPMM_KERNEL_WINDOW ||
+                          plan->kernel == SPMM_KERNEL_SMALLN;
   const Shape s = row_family ? choose_shape(plan->N, bf16, vector_ok) : choose_shape_balanced(plan->N, bf16, vector_ok);
   const bool window = plan->kernel == SPMM_KERNEL_WINDOW && s.G == 32 && s.nch == 1 && s.vec == (bf16 ? 8 : 4);
   Launch L{};
@@ -81,7 +82,10 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
   L.stream = stream;
 
   cudaError_t e;
-  if (window) {
+  if (plan->kernel == SPMM_KERNEL_SMALLN && plan->N <= 8) {
+    e = bf16 ? launch_rowgroup_bf16(L, plan->group_lanes) : launch_rowgroup_f32(L, plan->group_lanes);
+    if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+  } else if (window) {
     e = bf16 ? launch_window_bf16(L) : launch_window_f32(L);
     if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
   } else if (row_family) {
@@ -127,6 +131,31 @@ spmm_status sddmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const floa
   L.colind = colind;
   L.B = B;
   const cudaError_t e = launch_sddmm_f32(L, choose_shape_balanced(plan->N, false, vector_ok), Cd, out);
+  return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+}
+
+spmm_status semiring(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* vals, const float* B,
+                     float* C, int32_t add_op, int32_t mul_op, cudaStream_t stream) {
+  if (add_op < SPMM_ADD_SUM || add_op > SPMM_ADD_MAX || mul_op < SPMM_MUL_TIMES || mul_op > SPMM_MUL_PLUS)
+    return SPMM_ERR_INVALID_ARG;
+  const int sr = 2 * add_op + mul_op;
+  if (sr == 0) return exec(plan, K, colind, vals, B, false, C, stream);
+  if (!plan) return SPMM_ERR_PLAN_MISMATCH;
+  if (K < 0) return SPMM_ERR_INVALID_ARG;
+  if (plan->M == 0 || plan->N == 0) return SPMM_OK;
+  if (!C || (plan->nnz > 0 && (!colind || !vals || !B || K == 0))) return SPMM_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (!guard.ok) return SPMM_ERR_CUDA;
+  const bool vector_ok = plan->N % 4 == 0 && aligned16(B) && aligned16(C);
+  Launch L = plan_launch(plan, stream);
+  L.K = K;
+  L.colind = colind;
+  L.vals = vals;
+  L.B = B;
+  L.C = C;
+  cudaError_t e = launch_semiring_f32(L, choose_shape_balanced(plan->N, false, vector_ok), sr);
+  if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+  if (e == cudaSuccess) e = launch_fixup(L, sr);
   return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
 }
 
@@ -197,6 +226,11 @@ spmm_status spmm_csr_bf16f32(int32_t M, int32_t K, int32_t N, const int32_t* row
 spmm_status spmm_csr_sddmm_f32(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* C, const float* B,
                                float* out, void* stream) {
   return sddmm(plan, K, colind, C, B, out, static_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_csr_semiring_f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* vals,
+                                       const float* B, float* C, int32_t add_op, int32_t mul_op, void* stream) {
+  return semiring(plan, K, colind, vals, B, C, add_op, mul_op, static_cast<cudaStream_t>(stream));
 }
 
 spmm_status spmm_csr_fusedmm_f32(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* C,

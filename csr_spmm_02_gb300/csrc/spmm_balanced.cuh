@@ -86,7 +86,7 @@ __host__ __device__ constexpr size_t balanced_smem_layout_bytes(int W, int TW, i
          + 16;                     // mbarrier
 }
 
-template <typename BT, int VEC, int G, int NCH, bool FUSED>
+template <typename BT, int VEC, int G, int NCH, bool FUSED, int SR>
 __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::value)
     spmm_balanced_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr,
                          const int32_t* __restrict__ colind, const float* __restrict__ vals,
@@ -95,7 +95,9 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::v
                          int* __restrict__ err, const float* __restrict__ Cd, const float* __restrict__ Bd) {
   // FUSED: B is D (gathered and accumulated), Cd and Bd the SDDMM operands, vals
   // unused (its staging area holds the local row of every staged nonzero).
+  // SR: semiring code (spmm_device.cuh); 0 = ordinary SpMM.
   static_assert(!FUSED || sizeof(BT) == 4, "FusedMM is fp32");
+  static_assert(SR == 0 || (!FUSED && sizeof(BT) == 4), "semirings: fp32 SpMM only");
   using DotSlice = BSlice<float, FUSED ? VEC : 1>;  // fp32 slices of the dot-product operands
   constexpr int S = 32 / G;                // nonzeros per warp step
   constexpr int W = kThreads / 32;         // warps (workers) per CTA
@@ -260,14 +262,24 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::v
   };
   auto slot_ptr = [&](int worker, int ch) { return s_slot + worker * TW + (ch * G + gl) * VEC; };
   FVec<VEC> acc[NCH];
+  auto reset = [&](FVec<VEC>& a) {
+    if constexpr (SR == 0) a.zero(); else sr_reset<SR>(a);
+  };
+  // acc (+)= v (x) b for a slot that holds a nonzero of the current row (ok),
+  // unchanged otherwise (ordinary SpMM: v is already 0 for such slots)
+  auto apply = [&](FVec<VEC>& a, float v, bool ok, const FVec<VEC>& b) {
+    if constexpr (SR == 0) a.fma(pair(ok ? v : 0.f), b); else sr_apply<SR>(a, v, b, ok);
+  };
 #pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) acc[ch].zero();
+  for (int ch = 0; ch < NCH; ++ch) reset(acc[ch]);
   // Combine the S groups' partial rows: afterwards every group holds the sum.
   auto butterfly = [&] {
 #pragma unroll
     for (int o = G; o < 32; o <<= 1)
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) acc[ch].add_shfl_xor(o);
+      for (int ch = 0; ch < NCH; ++ch) {
+        if constexpr (SR == 0) acc[ch].add_shfl_xor(o); else sr_combine_shfl_xor<SR>(acc[ch], o);
+      }
   };
   auto store_row = [&](float* dst) {  // group 0 writes the row slice (streaming)
     if (grp == 0) {
@@ -295,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::v
       butterfly();
       if (began_before) park(r, kSlotHead); else store_row(crow0 + size_t(r) * N);
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) acc[ch].zero();
+      for (int ch = 0; ch < NCH; ++ch) reset(acc[ch]);
     } else {
       store_row(crow0 + size_t(r) * N);
     }
@@ -305,22 +317,24 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::v
   };
   // One step: the S groups take nonzeros a .. a+S-1 (group grp: n = a + grp,
   // value v, B slice b); rows ending inside the step are completed in order.
-  auto step = [&](int a, float v, const BSlice<BT, VEC> (&bs)[NCH]) {
+  auto step = [&](int a, float v, bool ok, const BSlice<BT, VEC> (&bs)[NCH]) {
     FVec<VEC> b[NCH];
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) bs[ch].widen(b[ch]);
     const int n = a + grp;
     int lo = a;
+    // (ordinary SpMM: slots without a nonzero of the row carry v = 0, so the
+    // row test alone masks them; other semirings also need `ok`)
     while (next_end <= a + S) {  // a row ends inside (or right after) this step
-      const float2 vv = pair((n >= lo && n < next_end) ? v : 0.f);
+      const bool in = (SR == 0 || ok) && n >= lo && n < next_end;
 #pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) acc[ch].fma(vv, b[ch]);
+      for (int ch = 0; ch < NCH; ++ch) apply(acc[ch], v, in, b[ch]);
       lo = next_end;
       end_row();
     }
-    const float2 vv = pair(n >= lo ? v : 0.f);
+    const bool in = (SR == 0 || ok) && n >= lo;
 #pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) acc[ch].fma(vv, b[ch]);
+    for (int ch = 0; ch < NCH; ++ch) apply(acc[ch], v, in, b[ch]);
   };
   int q = pw0;
   for (; q + U * S <= pw1; q += U * S) {  // full batches
@@ -346,12 +360,12 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::v
         for (int ch = 0; ch < NCH; ++ch) {
           FVec<VEC> b;
           bs[s][ch].widen(b);
-          acc[ch].fma(vv, b);
+          if constexpr (SR == 0) acc[ch].fma(vv, b); else sr_apply<SR>(acc[ch], value(s), b, true);
         }
       }
     } else {
 #pragma unroll
-      for (int s = 0; s < U; ++s) step(q + s * S, value(s), bs[s]);
+      for (int s = 0; s < U; ++s) step(q + s * S, value(s), true, bs[s]);
     }
   }
   if (q < pw1) {  // short last batch: slots past the sub-range re-read its last nonzero's row, value 0
@@ -370,9 +384,10 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::v
     for (int s = 0; s < U; ++s) {
       const int a = q + s * S;
       if (a >= pw1) break;
+      const bool ok = a + grp < pw1;
       float v;
-      if constexpr (FUSED) v = a + grp < pw1 ? fv[s] : 0.f; else v = a + grp < pw1 ? valw[a] : 0.f;
-      step(a, v, bs[s]);
+      if constexpr (FUSED) v = ok ? fv[s] : 0.f; else v = ok ? valw[a] : 0.f;
+      step(a, v, ok, bs[s]);
     }
   }
   while (r < rw1) end_row();  // rows ending exactly at the sub-range end (empty rows too)
@@ -393,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::v
       for (int ch = 0; ch < NCH; ++ch) {
         FVec<VEC> piece;
         piece.load_plain(slot_ptr(w2, ch));
-        acc[ch].add(piece);
+        if constexpr (SR == 0) acc[ch].add(piece); else sr_combine<SR>(acc[ch], piece);
       }
       if (m.y == kSlotHead) return true;
     }
@@ -404,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::v
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
       keep[ch] = acc[ch];
-      acc[ch].zero();
+      reset(acc[ch]);
     }
     walk(s_meta[0].x, 0);
     store_row(carry + size_t(cta) * 2 * N);  // slot 0: completed by the fixup
@@ -417,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::v
   }
 }
 
-template <typename BT, int VEC, int G, int NCH, bool FUSED = false>
+template <typename BT, int VEC, int G, int NCH, bool FUSED = false, int SR = 0>
 cudaError_t launch_balanced_t(const Launch& L, const float* Cd = nullptr, const float* Bd = nullptr) {
   constexpr int W = kThreads / 32;
   constexpr int TW = G * VEC * NCH;
@@ -427,13 +442,13 @@ cudaError_t launch_balanced_t(const Launch& L, const float* Cd = nullptr, const 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= kMaxDevices || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(spmm_balanced_kernel<BT, VEC, G, NCH, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(spmm_balanced_kernel<BT, VEC, G, NCH, FUSED, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(balanced_smem_layout_bytes(W, TW, kMaxItemsPerCta)));
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
   const dim3 grid(unsigned(L.num_ctas), unsigned((L.N + TW - 1) / TW));
-  spmm_balanced_kernel<BT, VEC, G, NCH, FUSED><<<grid, kThreads, smem, L.stream>>>(
+  spmm_balanced_kernel<BT, VEC, G, NCH, FUSED, SR><<<grid, kThreads, smem, L.stream>>>(
       L.M, L.N, L.rowptr, L.colind, L.vals, static_cast<const BT*>(L.B), L.C, L.part,
       L.items_per_cta, L.carry, L.err, Cd, Bd);
   return cudaGetLastError();

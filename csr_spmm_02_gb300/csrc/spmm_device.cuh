@@ -163,6 +163,75 @@ struct BSlice<uint16_t, 1> {
 __device__ __forceinline__ float2 pair(float v) { return make_float2(v, v); }
 
 // ---------------------------------------------------------------------------
+// Semirings: C[i][n] = (+) over row i of vals (x) B (the Sgap page's
+// generalised reduction, sparse-dense hybrid algebra, Eq. 3).  Code SR =
+// 2 * add + mul with add 0 sum, 1 min, 2 max and mul 0 multiply, 1 add;
+// SR = 0 is the ordinary SpMM, which keeps its packed-FMA path.
+// ---------------------------------------------------------------------------
+template <int SR>
+__device__ __forceinline__ float sr_identity() {
+  return SR / 2 == 0 ? 0.f : __int_as_float(SR / 2 == 1 ? 0x7f800000 : 0xff800000);  // 0, +inf, -inf
+}
+template <int SR>
+__device__ __forceinline__ float sr_plus(float a, float b) {
+  if constexpr (SR / 2 == 0) return a + b;
+  else if constexpr (SR / 2 == 1) return fminf(a, b);
+  else return fmaxf(a, b);
+}
+template <int SR>
+__device__ __forceinline__ float sr_times(float v, float b) {
+  if constexpr (SR % 2 == 0) return v * b;
+  else return v + b;
+}
+// Every element of `a` set to the identity of (+).
+template <int SR, int VEC>
+__device__ __forceinline__ void sr_reset(FVec<VEC>& a) {
+  if constexpr (VEC == 1) {
+    a.x = sr_identity<SR>();
+  } else {
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) a.p[j] = make_float2(sr_identity<SR>(), sr_identity<SR>());
+  }
+}
+// a (+)= v (x) b where `valid`, else unchanged.
+template <int SR, int VEC>
+__device__ __forceinline__ void sr_apply(FVec<VEC>& a, float v, const FVec<VEC>& b, bool valid) {
+  if constexpr (VEC == 1) {
+    a.x = valid ? sr_plus<SR>(a.x, sr_times<SR>(v, b.x)) : a.x;
+  } else {
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) {
+      const float x = sr_plus<SR>(a.p[j].x, sr_times<SR>(v, b.p[j].x));
+      const float y = sr_plus<SR>(a.p[j].y, sr_times<SR>(v, b.p[j].y));
+      a.p[j] = valid ? make_float2(x, y) : a.p[j];
+    }
+  }
+}
+// a (+)= o
+template <int SR, int VEC>
+__device__ __forceinline__ void sr_combine(FVec<VEC>& a, const FVec<VEC>& o) {
+  if constexpr (VEC == 1) {
+    a.x = sr_plus<SR>(a.x, o.x);
+  } else {
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) a.p[j] = make_float2(sr_plus<SR>(a.p[j].x, o.p[j].x), sr_plus<SR>(a.p[j].y, o.p[j].y));
+  }
+}
+// a (+)= the lane (lane ^ mask)'s a
+template <int SR, int VEC>
+__device__ __forceinline__ void sr_combine_shfl_xor(FVec<VEC>& a, int mask) {
+  if constexpr (VEC == 1) {
+    a.x = sr_plus<SR>(a.x, __shfl_xor_sync(0xffffffffu, a.x, mask));
+  } else {
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) {
+      a.p[j].x = sr_plus<SR>(a.p[j].x, __shfl_xor_sync(0xffffffffu, a.p[j].x, mask));
+      a.p[j].y = sr_plus<SR>(a.p[j].y, __shfl_xor_sync(0xffffffffu, a.p[j].y, mask));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // C stores (each C element is written once: streaming / evict-first)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void st_stream4(float* p, float x, float y, float z, float w) {

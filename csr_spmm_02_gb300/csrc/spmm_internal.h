@@ -37,6 +37,7 @@ struct spmm_plan_s {
   int32_t empty_rows = 0;
   int32_t items_per_cta = 0;  // balanced only
   int32_t num_ctas = 0;       // balanced only
+  int32_t group_lanes = 0;    // SMALLN only: lanes sharing a row
   int device = 0;
   bool stream_ordered = false;  // workspace from cudaMallocAsync (one-call form)
   // device workspace (one allocation, carved up)
@@ -81,17 +82,28 @@ Shape choose_shape(int32_t N, bool bf16, bool vector_ok, int chunks_f32);
 inline Shape choose_shape(int32_t N, bool bf16, bool vector_ok) {
   return choose_shape(N, bf16, vector_ok, SPMM_LANE_CHUNKS);
 }
+#ifndef SPMM_BAL_MAX_TW
+#define SPMM_BAL_MAX_TW 0
+#endif
 inline Shape choose_shape_balanced(int32_t N, bool bf16, bool vector_ok) {
-  return choose_shape(N, bf16, vector_ok, SPMM_BAL_CHUNKS);
+  Shape s = choose_shape(N, bf16, vector_ok, SPMM_BAL_CHUNKS);
+  if (SPMM_BAL_MAX_TW > 0)
+    while (s.G > 1 && s.tile_width() > SPMM_BAL_MAX_TW) s.G >>= 1;
+  return s;
 }
 
 cudaError_t launch_row_f32(const Launch& L, Shape s);
 cudaError_t launch_row_bf16(const Launch& L, Shape s);
 cudaError_t launch_balanced_f32(const Launch& L, Shape s);
 cudaError_t launch_balanced_bf16(const Launch& L, Shape s);
+cudaError_t launch_rowgroup_f32(const Launch& L, int lanes);
+cudaError_t launch_rowgroup_bf16(const Launch& L, int lanes);
 cudaError_t launch_window_f32(const Launch& L);
 cudaError_t launch_window_bf16(const Launch& L);
-cudaError_t launch_fixup(const Launch& L);
+cudaError_t launch_fixup(const Launch& L, int sr = 0);  // sr: semiring code, 0 = sum
+// Balanced kernel with a semiring (fp32 B); sr = 2 * add + mul in 1..5
+// (add 0 sum, 1 min, 2 max; mul 0 multiply, 1 add).
+cudaError_t launch_semiring_f32(const Launch& L, Shape s, int sr);
 cudaError_t launch_sddmm_f32(const Launch& L, Shape s, const float* Cd, float* out);
 cudaError_t launch_fusedmm_f32(const Launch& L, Shape s, const float* Cd, const float* Bd);
 // Merge-path coordinates of the P+1 range starts (ranges of T items) into part.

@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(kThreads) validate_kernel(const int32_t* __res
 // One warp per CTA range c.  If a row starts inside range c and its end item
 // lies in a later range (carry slot 1 of c), add slot 1 of c and slot 0 of
 // every following range up to the one holding the row's end, in range order,
-// and write the C row.
+// and write the C row.  SR: the semiring whose (+) combines the pieces.
+template <int SR>
 __global__ void __launch_bounds__(kThreads) spmm_fixup_kernel(int32_t M, int32_t N,
                                                               const int32_t* __restrict__ rowptr,
                                                               const int2* __restrict__ part, int32_t P,
@@ -87,15 +88,21 @@ __global__ void __launch_bounds__(kThreads) spmm_fixup_kernel(int32_t M, int32_t
   while (__ldg(part + last + 1).x == row) ++last;  // range `last` holds the row's end item
   for (int n = lane; n < N; n += 32) {
     float s = carry[(size_t(c) * 2 + 1) * N + n];
-    for (int c2 = c + 1; c2 <= last; ++c2) s += carry[(size_t(c2) * 2) * N + n];
+    for (int c2 = c + 1; c2 <= last; ++c2) s = sr_plus<SR>(s, carry[(size_t(c2) * 2) * N + n]);
     st_stream1(C + size_t(row) * N + n, s);
   }
 }
 
-cudaError_t launch_fixup(const Launch& L) {
+cudaError_t launch_fixup(const Launch& L, int sr) {
   constexpr int kWarps = kThreads / 32;
   const unsigned grid = unsigned((L.num_ctas + kWarps - 1) / kWarps);
-  spmm_fixup_kernel<<<grid, kThreads, 0, L.stream>>>(L.M, L.N, L.rowptr, L.part, L.num_ctas, L.carry, L.C);
+  switch (sr) {
+#define SPMM_FIXUP_CASE(X) \
+  case X: spmm_fixup_kernel<X><<<grid, kThreads, 0, L.stream>>>(L.M, L.N, L.rowptr, L.part, L.num_ctas, L.carry, L.C); break;
+    SPMM_FIXUP_CASE(0) SPMM_FIXUP_CASE(1) SPMM_FIXUP_CASE(2) SPMM_FIXUP_CASE(3) SPMM_FIXUP_CASE(4) SPMM_FIXUP_CASE(5)
+#undef SPMM_FIXUP_CASE
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
@@ -136,7 +143,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   if (M < 0 || N < 0 || nnz < 0) return SPMM_ERR_INVALID_ARG;
   if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
   if (M > 0 && !rowptr) return SPMM_ERR_INVALID_ARG;
-  if (kernel < SPMM_KERNEL_AUTO || kernel > SPMM_KERNEL_WINDOW) return SPMM_ERR_INVALID_ARG;
+  if (kernel < SPMM_KERNEL_AUTO || kernel > SPMM_KERNEL_SMALLN) return SPMM_ERR_INVALID_ARG;
   if (items_per_cta != 0 && (items_per_cta < 256 || items_per_cta > kMaxItemsPerCta || items_per_cta % 256 != 0))
     return SPMM_ERR_INVALID_ARG;
 
@@ -189,6 +196,16 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
     // Rows wide enough for a warp per column tile: the window kernel (it
     // falls back to per-row gathers where the columns are scattered).
     if (plan->kernel == SPMM_KERNEL_ROW && N >= 128) plan->kernel = SPMM_KERNEL_WINDOW;
+    // Narrow B: a whole output row fits a lane; several lanes share a row.
+    if (plan->kernel == SPMM_KERNEL_ROW && N <= 8) plan->kernel = SPMM_KERNEL_SMALLN;
+  }
+  if (plan->kernel == SPMM_KERNEL_SMALLN) {
+    // r lanes per row so that each lane takes about 4 nonzeros of a mean row
+    // (4 gathers in flight per lane), between 2 and 32.
+    const double mean = M > 0 ? double(nnz) / double(M) : 0.0;
+    int r = 2;
+    while (r < 32 && 4.0 * r < mean) r <<= 1;
+    plan->group_lanes = r;
   }
 
   {  // merge-path partition and carry rows: used by the balanced SpMM, SDDMM and FusedMM
@@ -246,6 +263,15 @@ spmm_status spmm_plan_get_info(spmm_plan_t plan, spmm_plan_info* info) {
   info->items_per_cta = plan->items_per_cta;
   info->num_ctas = plan->num_ctas;
   info->workspace_bytes = plan->workspace_bytes;
+  info->group_lanes = plan->group_lanes;
+  return SPMM_OK;
+}
+
+spmm_status spmm_plan_set_group_lanes(spmm_plan_t plan, int32_t lanes) {
+  if (!plan) return SPMM_ERR_PLAN_MISMATCH;
+  if (plan->kernel != SPMM_KERNEL_SMALLN) return SPMM_ERR_INVALID_ARG;
+  if (lanes != 2 && lanes != 4 && lanes != 8 && lanes != 16 && lanes != 32) return SPMM_ERR_INVALID_ARG;
+  plan->group_lanes = lanes;
   return SPMM_OK;
 }
 

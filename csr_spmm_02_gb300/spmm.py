@@ -31,13 +31,14 @@ SPMM_OK = 0
 STATUS_NAMES = {0: "SPMM_OK", 1: "SPMM_ERR_INVALID_ARG", 2: "SPMM_ERR_INVALID_CSR",
                 3: "SPMM_ERR_UNSUPPORTED", 4: "SPMM_ERR_PLAN_MISMATCH", 5: "SPMM_ERR_CUDA",
                 6: "SPMM_ERR_DEVICE_TIMEOUT"}
-KERNELS = {"auto": 0, "row": 1, "balanced": 2, "window": 3}
-KERNEL_NAMES = {1: "row", 2: "balanced", 3: "window"}
+KERNELS = {"auto": 0, "row": 1, "balanced": 2, "window": 3, "smalln": 4}
+KERNEL_NAMES = {1: "row", 2: "balanced", 3: "window", 4: "smalln"}
 
 EXPORTS = ["spmm_csr_plan", "spmm_csr_plan_ex", "spmm_plan_get_info", "spmm_plan_destroy",
            "spmm_csr_f32_exec", "spmm_csr_bf16f32_exec", "spmm_csr_f32", "spmm_csr_bf16f32",
            "spmm_csr_validate", "spmm_plan_check_device", "spmm_plan_set_split_event",
-           "spmm_csr_f32_noalloc", "spmm_csr_sddmm_f32", "spmm_csr_fusedmm_f32", "spmm_status_string"]
+           "spmm_csr_f32_noalloc", "spmm_csr_sddmm_f32", "spmm_csr_fusedmm_f32", "spmm_csr_semiring_f32_exec",
+           "spmm_plan_set_group_lanes", "spmm_status_string"]
 
 
 class SpmmError(RuntimeError):
@@ -50,7 +51,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("M", ctypes.c_int32), ("nnz", ctypes.c_int64),
                 ("N", ctypes.c_int32), ("max_row_nnz", ctypes.c_int32), ("empty_rows", ctypes.c_int32),
                 ("items_per_cta", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("group_lanes", ctypes.c_int32)]
 
 
 _lib = None
@@ -85,6 +86,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "spmm_csr_f32_noalloc": [i32, i32, i32, i64, vp, vp, vp, vp, vp, vp],
         "spmm_csr_sddmm_f32": [vp, i32, vp, vp, vp, vp, vp],
         "spmm_csr_fusedmm_f32": [vp, i32, vp, vp, vp, vp, vp, vp],
+        "spmm_csr_semiring_f32_exec": [vp, i32, vp, vp, vp, vp, i32, i32, vp],
+        "spmm_plan_set_group_lanes": [vp, i32],
         "spmm_status_string": [ctypes.c_int],
     }
     for name, args in sig.items():
@@ -194,6 +197,27 @@ def spmm_csr_sddmm_f32(plan: Plan, K, colind, C, B, out, stream=None):
                                      _ptr(B, _F32, "B", True), _ptr(out, _F32, "out", True), _stream(stream)),
            "spmm_csr_sddmm_f32")
     return out
+
+
+def spmm_plan_set_group_lanes(plan: Plan, lanes: int):
+    """Lanes (2, 4, 8, 16, 32) that share a row in a SMALLN plan."""
+    _check(load().spmm_plan_set_group_lanes(plan.handle, lanes), "spmm_plan_set_group_lanes")
+
+
+ADD_OPS = {"sum": 0, "min": 1, "max": 2}
+MUL_OPS = {"mul": 0, "add": 1}
+
+
+def spmm_csr_semiring_f32_exec(plan: Plan, K, colind, vals, B, C, add="sum", mul="mul", stream=None):
+    """C[i, n] = add-reduction over row i of vals[p] mul B[colind[p], n] (fp32).
+
+    add in {"sum", "min", "max"}, mul in {"mul", "add"}; an empty row gives the
+    identity of add (0, +inf, -inf)."""
+    _check(load().spmm_csr_semiring_f32_exec(plan.handle, K, _ptr(colind, _I32, "colind", True),
+                                             _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True),
+                                             _ptr(C, _F32, "C"), ADD_OPS[add], MUL_OPS[mul], _stream(stream)),
+           "spmm_csr_semiring_f32_exec")
+    return C
 
 
 def spmm_csr_fusedmm_f32(plan: Plan, K, colind, C, B, D, E, stream=None):

@@ -82,7 +82,7 @@ typedef enum {
   SPMM_KERNEL_AUTO = 0,      /* chosen from the row-length statistics */
   SPMM_KERNEL_ROW = 1,       /* one (sub-)warp group per row: short, uniform rows */
   SPMM_KERNEL_BALANCED = 2,  /* merge-path nnz-balanced split + fixup: skewed rows */
-  SPMM_KERNEL_WINDOW = 3     /* short rows, B rows reused across rows: a CTA of 32 rows
+  SPMM_KERNEL_WINDOW = 3,    /* short rows, B rows reused across rows: a CTA of 32 rows
                               * whose columns span few enough B rows stages them in
                               * shared memory and reuses each from registers for 4
                               * rows; other CTAs gather as the row kernel.  Runs when a
@@ -91,6 +91,11 @@ typedef enum {
                               * aligned B and C); otherwise exec runs the row kernel.
                               * Absent entries inside the window are multiplied as
                               * zeros, so a NaN/Inf in such a B row reaches the row. */
+  SPMM_KERNEL_SMALLN = 4     /* N <= 8: a group of r lanes shares each row, every lane
+                              * holding the whole output row (the Sgap page's
+                              * {<1/g row, c col>, r} point, atomic parallelism, Table 1);
+                              * r from the plan (spmm_plan_set_group_lanes overrides).
+                              * For N > 8 exec runs the row kernel instead. */
 } spmm_kernel;
 
 /* Opaque plan: owns its device workspace (merge-path partition, carry rows
@@ -108,6 +113,7 @@ typedef struct {
   int32_t items_per_cta;   /* balanced: merge-path items (row ends + nonzeros) per CTA */
   int32_t num_ctas;        /* balanced: number of merge-path ranges (CTAs) */
   int64_t workspace_bytes; /* device bytes the plan owns */
+  int32_t group_lanes;     /* SMALLN: lanes r that share a row (2..32) */
 } spmm_plan_info;
 
 /*
@@ -132,6 +138,10 @@ SPMM_API spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz
 SPMM_API spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
                              int32_t kernel, int32_t items_per_cta, void* stream,
                              spmm_plan_t* plan_out);
+
+/* Set the lanes r (2, 4, 8, 16 or 32) that share a row in the SMALLN kernel;
+ * SPMM_ERR_INVALID_ARG for another value or a plan of another kernel. */
+SPMM_API spmm_status spmm_plan_set_group_lanes(spmm_plan_t plan, int32_t lanes);
 
 /* Copy the plan's decisions into *info (host memory).  Every plan also holds
  * the merge-path partition used by the balanced SpMM, SDDMM and FusedMM. */
@@ -172,6 +182,33 @@ SPMM_API spmm_status spmm_csr_sddmm_f32(spmm_plan_t plan, int32_t K, const int32
  * B and D are K x N, E is M x N (fp32, row-major, N the plan's width).  Runs
  * the nnz-balanced kernel and its fixup; deterministic for a given plan.
  */
+/* Operators of the semiring form below. */
+typedef enum {
+  SPMM_ADD_SUM = 0,  /* (+) = addition, identity 0 */
+  SPMM_ADD_MIN = 1,  /* (+) = minimum, identity +infinity */
+  SPMM_ADD_MAX = 2   /* (+) = maximum, identity -infinity */
+} spmm_add_op;
+typedef enum {
+  SPMM_MUL_TIMES = 0, /* (x) = multiplication */
+  SPMM_MUL_PLUS = 1   /* (x) = addition (with SPMM_ADD_MIN: the tropical semiring) */
+} spmm_mul_op;
+
+/*
+ * Semiring SpMM (page "Sgap: Towards Efficient Sparse Tensor Algebra
+ * Compilation for GPU", sparse-dense hybrid algebra, Eq. 3, where the
+ * reduction's (+) may be any commutative operation and (x) any binary one):
+ * C[i][n] = (+) over the stored p of row i of vals[p] (x) B[colind[p]][n],
+ * with an empty row giving the identity of (+).  fp32 B and C, arguments as
+ * in spmm_csr_f32_exec.  (SUM, TIMES) is the ordinary SpMM and runs the
+ * plan's own kernel; any other pair runs the nnz-balanced kernel and its
+ * fixup with that (+) and (x).  min and max are exact in any order, so those
+ * results are bitwise the binary32 rounding of the exact value; sums carry
+ * fp32 rounding.  SPMM_ERR_INVALID_ARG for an unknown operator.
+ */
+SPMM_API spmm_status spmm_csr_semiring_f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind,
+                                                const float* vals, const float* B, float* C,
+                                                int32_t add_op, int32_t mul_op, void* stream);
+
 SPMM_API spmm_status spmm_csr_fusedmm_f32(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* C,
                                           const float* B, const float* D, float* E, void* stream);
 

@@ -10,7 +10,7 @@ from tests import oracle_pins
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["row", "balanced", "window"]
+KERNELS = ["row", "balanced", "window", "smalln"]
 
 
 def mixed(seed, M=1500, K=900, N=64, b_dtype="f32", integer=False, duplicates=False):
