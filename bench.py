@@ -110,11 +110,24 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The sources that define each timed kernel (what a traffic record depends on).
+KERNEL_SOURCES = {
+    "row": ["spmm_row.cuh", "spmm_row_f32.cu", "spmm_row_bf16.cu"],
+    "balanced": ["spmm_balanced.cuh", "spmm_balanced_f32.cu", "spmm_balanced_bf16.cu", "spmm_sddmm.cuh",
+                 "spmm_plan.cu"],
+    "window": ["spmm_window.cuh", "spmm_window.cu"],
+    "smalln": ["spmm_rowgroup.cuh", "spmm_rowgroup.cu"],
+    "sddmm": ["spmm_sddmm.cuh", "spmm_sddmm_f32.cu"],
+    "fusedmm": ["spmm_balanced.cuh", "spmm_fusedmm_f32.cu", "spmm_sddmm.cuh", "spmm_plan.cu"],
+}
+COMMON_SOURCES = ["spmm_device.cuh", "spmm_internal.h", "spmm_api.cu"]
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "csr_spmm_02_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES.get(kernel, []) + COMMON_SOURCES):
+        with open(os.path.join(ROOT, "csr_spmm_02_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -126,7 +139,7 @@ def ncu_traffic(workload: str, kernel: str):
             rec = json.load(f)["captures"][workload][kernel]
     except Exception:
         return None
-    if rec.get("source_hash") != kernel_source_hash():
+    if rec.get("source_hash") != kernel_source_hash(kernel):
         return None
     return int(rec["dram_bytes_per_launch"])
 
@@ -219,7 +232,7 @@ def oracle_rows_block(p, start, count):
     return np.arange(start, start + count, dtype=np.int32)
 
 
-def time_oracle(p, seconds: float, op="spmm", dense=None):
+def time_oracle(p, seconds: float, op="spmm", dense=None, semiring=("sum", "mul")):
     """Run the oracle over consecutive row blocks (wrapping) for ~`seconds`.
 
     Returns (GFLOP/s, description of the sample)."""
@@ -234,7 +247,11 @@ def time_oracle(p, seconds: float, op="spmm", dense=None):
     while spent < seconds:
         count = min(block, p.M - start)
         t0 = time.perf_counter()
-        if op == "spmm":
+        if op == "spmm" and semiring != ("sum", "mul"):
+            rp = p.rowptr[start:start + count + 1]
+            sl = slice(int(rp[0]), int(rp[-1]))
+            oracle.semiring_reference((rp - rp[0]).astype(np.int32), p.colind[sl], p.vals[sl], p.B, *semiring)
+        elif op == "spmm":
             rows = oracle_rows_block(p, start, count)
             oracle.spmm_reference(p.rowptr, p.colind, p.vals, p.B, b_dtype=p.b_dtype, rows=rows, with_bound=False)
         else:
@@ -259,10 +276,11 @@ def reference_arm(args, p, cfg):
     """--impl reference: the CPU oracle, K timed steps of a bounded sample each."""
     import numpy as np
     import oracle
-    if args.op != "spmm":
+    if args.op != "spmm" or args.semiring != ("sum", "mul"):
         steps = args.steps if args.steps is not None else 3
-        dense = op_dense_inputs(p, args.op)
-        runs = [time_oracle(p, 0.5, args.op, dense) for _ in range(max(args.warmup, 0) + steps)][args.warmup:]
+        dense = op_dense_inputs(p, args.op) if args.op != "spmm" else None
+        runs = [time_oracle(p, 0.5, args.op, dense, args.semiring)
+                for _ in range(max(args.warmup, 0) + steps)][args.warmup:]
         value = sum(r[0] for r in runs) / len(runs)
         return {
             "impl": "reference", "metric": OP_METRIC[args.op], "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -339,6 +357,8 @@ def gpu_arm(args, p, cfg, ws, rank, local):
     t0 = time.perf_counter()
     plan = spmm.spmm_csr_plan(rowptr, p.M, p.nnz, p.N, kernel=args.kernel if op == "spmm" else "auto",
                               items_per_cta=args.items_per_cta)
+    if args.group_lanes:
+        spmm.spmm_plan_set_group_lanes(plan, args.group_lanes)
     torch.cuda.synchronize()
     plan_ms = (time.perf_counter() - t0) * 1e3
     info = plan.info()
@@ -346,9 +366,15 @@ def gpu_arm(args, p, cfg, ws, rank, local):
         run = spmm.spmm_csr_bf16f32_exec if bf16 else spmm.spmm_csr_f32_exec
         kernel = info["kernel"]
         launches_per_step = 2 if kernel == "balanced" else 1
+        if args.semiring != ("sum", "mul"):
+            assert not bf16, "semirings take fp32 B"
+            kernel, launches_per_step = "balanced", 2
 
-        def step(t=d):
-            run(plan, p.K, t["colind"], t["vals"], t["B"], out)
+            def step(t=d):
+                spmm.spmm_csr_semiring_f32_exec(plan, p.K, t["colind"], t["vals"], t["B"], out, *args.semiring)
+        else:
+            def step(t=d):
+                run(plan, p.K, t["colind"], t["vals"], t["B"], out)
     elif op == "sddmm":
         kernel, launches_per_step = "sddmm", 1
 
@@ -459,7 +485,7 @@ def gpu_arm(args, p, cfg, ws, rank, local):
 
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
-        val, desc, _ = time_oracle(p, args.cpu_seconds, op, None if op == "spmm" else (Ch, Bh, Dh))
+        val, desc, _ = time_oracle(p, args.cpu_seconds, op, None if op == "spmm" else (Ch, Bh, Dh), args.semiring)
         cpu = {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
 
     cfg = dict(cfg)
@@ -496,18 +522,32 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=gen.WORKLOAD_ORDER, default="uniform64k")
     ap.add_argument("--op", choices=["spmm", "sddmm", "fusedmm"], default="spmm")
-    ap.add_argument("--kernel", choices=["auto", "row", "balanced", "window"], default="auto")
+    ap.add_argument("--kernel", choices=["auto", "row", "balanced", "window", "smalln"], default="auto")
+    ap.add_argument("--n", type=int, default=0, help="dense width: redraw B with this many columns")
+    ap.add_argument("--semiring", default="sum,mul", help="(+),(x): sum|min|max , mul|add (SpMM only)")
+    ap.add_argument("--group-lanes", type=int, default=0, help="lanes per row of a smalln plan")
     ap.add_argument("--items-per-cta", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
+    args.semiring = tuple(args.semiring.split(","))
 
     ws, rank, local = dist_env()
     if args.impl == "reference" and rank != 0:
         return 0  # rank 0 alone times the CPU oracle
     p = gen.make_workload(args.workload)
-    cfg = {"workload": args.workload if args.op == "spmm" else f"{args.workload} pattern, {args.op}", "M": p.M, "K": p.K, "N": p.N, "nnz": p.nnz, "b_dtype": p.b_dtype,
+    if args.n:  # same pattern and values, B redrawn with another width
+        import dataclasses
+        import numpy as np
+        B = gen.uniform_b(np.random.default_rng(1000 + p.seed), p.K, args.n, p.b_dtype)
+        p = dataclasses.replace(p, N=args.n, B=B, name=f"{p.name}_n{args.n}")
+    name = args.workload if args.op == "spmm" else f"{args.workload} pattern, {args.op}"
+    if args.n:
+        name += f", B redrawn with N={args.n}"
+    if args.semiring != ("sum", "mul"):
+        name += f", semiring ({args.semiring[0]}, {args.semiring[1]})"
+    cfg = {"workload": name, "M": p.M, "K": p.K, "N": p.N, "nnz": p.nnz, "b_dtype": p.b_dtype,
            "seed": p.seed, "compulsory_bytes": op_bytes(p, args.op)}
     if args.impl == "reference":
         print(json.dumps(reference_arm(args, p, cfg)), flush=True)
