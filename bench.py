@@ -116,6 +116,7 @@ KERNEL_SOURCES = {
     "balanced": ["spmm_balanced.cuh", "spmm_balanced_f32.cu", "spmm_balanced_bf16.cu", "spmm_sddmm.cuh",
                  "spmm_plan.cu"],
     "window": ["spmm_window.cuh", "spmm_window.cu"],
+    "window_tc": ["spmm_tc_window.cuh", "spmm_tc_window.cu"],
     "smalln": ["spmm_rowgroup.cuh", "spmm_rowgroup.cu"],
     "sddmm": ["spmm_sddmm.cuh", "spmm_sddmm_f32.cu"],
     "fusedmm": ["spmm_balanced.cuh", "spmm_fusedmm_f32.cu", "spmm_sddmm.cuh", "spmm_plan.cu"],
@@ -522,7 +523,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=gen.WORKLOAD_ORDER, default="uniform64k")
     ap.add_argument("--op", choices=["spmm", "sddmm", "fusedmm"], default="spmm")
-    ap.add_argument("--kernel", choices=["auto", "row", "balanced", "window", "smalln"], default="auto")
+    ap.add_argument("--kernel", choices=["auto", "row", "balanced", "window", "smalln", "window_tc"], default="auto")
     ap.add_argument("--n", type=int, default=0, help="dense width: redraw B with this many columns")
     ap.add_argument("--semiring", default="sum,mul", help="(+),(x): sum|min|max , mul|add (SpMM only)")
     ap.add_argument("--group-lanes", type=int, default=0, help="lanes per row of a smalln plan")

@@ -61,9 +61,12 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
 
   const bool vector_ok = plan->N % (bf16 ? 8 : 4) == 0 && aligned16(B) && aligned16(C);
   const bool row_family = plan->kernel == SPMM_KERNEL_ROW || plan->kernel == SPMM_KERNEL_WINDOW ||
-                          plan->kernel == SPMM_KERNEL_SMALLN;
+                          plan->kernel == SPMM_KERNEL_SMALLN || plan->kernel == SPMM_KERNEL_WINDOW_TC;
   const Shape s = row_family ? choose_shape(plan->N, bf16, vector_ok) : choose_shape_balanced(plan->N, bf16, vector_ok);
-  const bool window = plan->kernel == SPMM_KERNEL_WINDOW && s.G == 32 && s.nch == 1 && s.vec == (bf16 ? 8 : 4);
+  const bool window_family = plan->kernel == SPMM_KERNEL_WINDOW || plan->kernel == SPMM_KERNEL_WINDOW_TC;
+  const bool window = window_family && s.G == 32 && s.nch == 1 && s.vec == (bf16 ? 8 : 4);
+  const bool window_tc = plan->kernel == SPMM_KERNEL_WINDOW_TC && bf16 && plan->N % 16 == 0 && plan->N <= 256 &&
+                         aligned16(B) && aligned16(C);
   Launch L{};
   L.M = plan->M;
   L.N = plan->N;
@@ -84,6 +87,9 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
   cudaError_t e;
   if (plan->kernel == SPMM_KERNEL_SMALLN && plan->N <= 8) {
     e = bf16 ? launch_rowgroup_bf16(L, plan->group_lanes) : launch_rowgroup_f32(L, plan->group_lanes);
+    if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+  } else if (window_tc) {
+    e = launch_tc_window_bf16(L);
     if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
   } else if (window) {
     e = bf16 ? launch_window_bf16(L) : launch_window_f32(L);

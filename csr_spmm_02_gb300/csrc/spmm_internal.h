@@ -98,6 +98,7 @@ cudaError_t launch_balanced_f32(const Launch& L, Shape s);
 cudaError_t launch_balanced_bf16(const Launch& L, Shape s);
 cudaError_t launch_rowgroup_f32(const Launch& L, int lanes);
 cudaError_t launch_rowgroup_bf16(const Launch& L, int lanes);
+cudaError_t launch_tc_window_bf16(const Launch& L);
 cudaError_t launch_window_f32(const Launch& L);
 cudaError_t launch_window_bf16(const Launch& L);
 cudaError_t launch_fixup(const Launch& L, int sr = 0);  // sr: semiring code, 0 = sum

@@ -143,7 +143,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   if (M < 0 || N < 0 || nnz < 0) return SPMM_ERR_INVALID_ARG;
   if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
   if (M > 0 && !rowptr) return SPMM_ERR_INVALID_ARG;
-  if (kernel < SPMM_KERNEL_AUTO || kernel > SPMM_KERNEL_SMALLN) return SPMM_ERR_INVALID_ARG;
+  if (kernel < SPMM_KERNEL_AUTO || kernel > SPMM_KERNEL_WINDOW_TC) return SPMM_ERR_INVALID_ARG;
   if (items_per_cta != 0 && (items_per_cta < 256 || items_per_cta > kMaxItemsPerCta || items_per_cta % 256 != 0))
     return SPMM_ERR_INVALID_ARG;
 
@@ -193,9 +193,10 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
     // merge-path split bounds every CTA's work.
     const double mean = double(nnz) / double(M);
     plan->kernel = double(plan->max_row_nnz) <= 4.0 * mean + 32.0 ? SPMM_KERNEL_ROW : SPMM_KERNEL_BALANCED;
-    // Rows wide enough for a warp per column tile: the window kernel (it
-    // falls back to per-row gathers where the columns are scattered).
-    if (plan->kernel == SPMM_KERNEL_ROW && N >= 128) plan->kernel = SPMM_KERNEL_WINDOW;
+    // Rows wide enough for a warp per column tile: the window kernels (they
+    // fall back to per-row gathers where the columns are scattered); the
+    // tensor-core form where B is bf16 and N fits one MMA, else CUDA cores.
+    if (plan->kernel == SPMM_KERNEL_ROW && N >= 128) plan->kernel = SPMM_KERNEL_WINDOW_TC;
     // Narrow B: a whole output row fits a lane; several lanes share a row.
     if (plan->kernel == SPMM_KERNEL_ROW && N <= 8) plan->kernel = SPMM_KERNEL_SMALLN;
   }

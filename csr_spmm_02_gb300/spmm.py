@@ -31,8 +31,8 @@ SPMM_OK = 0
 STATUS_NAMES = {0: "SPMM_OK", 1: "SPMM_ERR_INVALID_ARG", 2: "SPMM_ERR_INVALID_CSR",
                 3: "SPMM_ERR_UNSUPPORTED", 4: "SPMM_ERR_PLAN_MISMATCH", 5: "SPMM_ERR_CUDA",
                 6: "SPMM_ERR_DEVICE_TIMEOUT"}
-KERNELS = {"auto": 0, "row": 1, "balanced": 2, "window": 3, "smalln": 4}
-KERNEL_NAMES = {1: "row", 2: "balanced", 3: "window", 4: "smalln"}
+KERNELS = {"auto": 0, "row": 1, "balanced": 2, "window": 3, "smalln": 4, "window_tc": 5}
+KERNEL_NAMES = {1: "row", 2: "balanced", 3: "window", 4: "smalln", 5: "window_tc"}
 
 EXPORTS = ["spmm_csr_plan", "spmm_csr_plan_ex", "spmm_plan_get_info", "spmm_plan_destroy",
            "spmm_csr_f32_exec", "spmm_csr_bf16f32_exec", "spmm_csr_f32", "spmm_csr_bf16f32",

@@ -91,11 +91,18 @@ typedef enum {
                               * aligned B and C); otherwise exec runs the row kernel.
                               * Absent entries inside the window are multiplied as
                               * zeros, so a NaN/Inf in such a B row reaches the row. */
-  SPMM_KERNEL_SMALLN = 4     /* N <= 8: a group of r lanes shares each row, every lane
+  SPMM_KERNEL_SMALLN = 4,    /* N <= 8: a group of r lanes shares each row, every lane
                               * holding the whole output row (the Sgap page's
                               * {<1/g row, c col>, r} point, atomic parallelism, Table 1);
                               * r from the plan (spmm_plan_set_group_lanes overrides).
                               * For N > 8 exec runs the row kernel instead. */
+  SPMM_KERNEL_WINDOW_TC = 5  /* the window kernel's dense product on the tensor cores
+                              * (tcgen05, accumulator in tensor memory) for bf16 B with
+                              * N a multiple of 16 up to 256: 128 rows per CTA, A's fp32
+                              * values split exactly into three bf16 terms, the window
+                              * walked in 64-column chunks; tiles with a span over 256
+                              * columns or duplicate columns gather per row.  Other B
+                              * types or widths run the window kernel. */
 } spmm_kernel;
 
 /* Opaque plan: owns its device workspace (merge-path partition, carry rows

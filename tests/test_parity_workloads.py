@@ -44,8 +44,8 @@ def test_workload_parity(name):
     rows = sample_rows(p, rng)
     C_ref, S = H.reference(p, rows=rows)
     a = H.device_arrays(p)
-    expect_kernel = {"uniform1k": "row", "uniform64k": "row", "banded": "window"}.get(name, "balanced")
-    others = {"row": ("balanced",), "window": ("row", "balanced"), "balanced": ("row",)}[expect_kernel]
+    expect_kernel = {"uniform1k": "row", "uniform64k": "row", "banded": "window_tc"}.get(name, "balanced")
+    others = {"row": ("balanced",), "window_tc": ("window", "row", "balanced"), "balanced": ("row",)}[expect_kernel]
     for kernel in ("auto",) + others:
         C, plan = H.run(p, kernel=kernel, arrays=a)
         if kernel == "auto":

@@ -1,7 +1,10 @@
-"""The window kernel (B rows staged per CTA, reused across 4 rows per warp)
-vs the CPU oracle: both of its paths (window and gather), the boundary
-between them, duplicates and unsorted columns, CTAs too large to stage,
-empty CTAs, several column tiles, determinism."""
+"""The window kernels vs the CPU oracle.  CUDA-core window (B rows staged per
+CTA, reused across 4 rows per warp): both of its paths (window and gather),
+the boundary between them, duplicates and unsorted columns, CTAs too large
+to stage, empty CTAs, several column tiles, determinism.  Tensor-core window
+(bf16 B, 128-row tiles, tcgen05): spans of one to four 64-column chunks and
+beyond (gather path), N from 16 to 256, ragged M, K inside the last chunk,
+duplicates and unsorted rows (gather path), exact integer products."""
 import numpy as np
 import pytest
 import torch
@@ -64,7 +67,7 @@ def check(p, kernel="window"):
 def test_banded_parity(b_dtype, N):
     p = banded(N, 1000, 1000, 32, 31, N, b_dtype=b_dtype)
     _, info = check(p, kernel="auto")
-    assert info["kernel"] == "window"
+    assert info["kernel"] == "window_tc"  # bf16 runs on the tensor cores, fp32 on the CUDA-core window
 
 
 @pytest.mark.parametrize("width", [95, 96, 97])  # CTA spans of 127, 128 and 129 B rows
@@ -114,4 +117,60 @@ def test_deterministic():
     p = banded(12, 2000, 2000, 32, 31, 256, b_dtype="bf16")
     C1, _ = H.run(p, kernel="window")
     C2, _ = H.run(p, kernel="window")
+    assert torch.equal(C1, C2)
+
+
+# ---- tensor-core window ----------------------------------------------------
+
+@pytest.mark.parametrize("N", [16, 32, 48, 128, 256])
+def test_tc_banded_parity(N):
+    p = banded(N + 500, 1000, 1000, 32, 31, N, b_dtype="bf16")
+    _, info = check(p, kernel="window_tc")
+    assert info["kernel"] == "window_tc"
+
+
+@pytest.mark.parametrize("below,above", [(0, 0), (10, 20), (60, 3), (100, 90), (150, 150)])
+def test_tc_spans_and_gather_fallback(below, above):
+    # 128-row tiles span 128 + below + above columns: 2 .. 4 chunks, then the gather path
+    p = banded(below + above, 777, 900, below, above, 64, b_dtype="bf16")
+    check(p, kernel="window_tc")
+
+
+@pytest.mark.parametrize("N", [16, 256])
+def test_tc_integer_exact(N):
+    p = banded(N + 1, 700, 740, 40, 21, N, b_dtype="bf16", integer=True, empty_every=9)
+    C, _ = H.run(p, kernel="window_tc")
+    C_ref, _ = H.reference(p)
+    H.assert_exact(C, C_ref, f"window_tc/N={N}")
+
+
+def test_tc_small_k_and_ragged_tail():
+    p = banded(3, 200, 70, 16, 16, 32, b_dtype="bf16")  # K = 70: the window ends inside a chunk
+    check(p, kernel="window_tc")
+    q = banded(4, 129, 129, 5, 5, 16, b_dtype="bf16")  # last tile holds one row
+    check(q, kernel="window_tc")
+
+
+def test_tc_duplicates_and_unsorted_use_gather():
+    p = banded(5, 600, 600, 8, 8, 64, b_dtype="bf16", integer=True, duplicates=True)
+    C, _ = H.run(p, kernel="window_tc")
+    H.assert_exact(C, H.reference(p)[0], "duplicates")
+    q = banded(6, 600, 600, 8, 8, 64, b_dtype="bf16", integer=True, unsorted=True)
+    C, _ = H.run(q, kernel="window_tc")
+    H.assert_exact(C, H.reference(q)[0], "unsorted")
+
+
+def test_tc_empty_tiles_and_fp32_fallback():
+    p = banded(7, 128 * 5 + 3, 300, 3, 3, 256, b_dtype="bf16", sparse_every=200)  # tiles 1, 3 empty
+    C, _ = check(p, kernel="window_tc")
+    empty = np.flatnonzero(np.diff(p.rowptr) == 0)
+    assert not bool(C[torch.from_numpy(empty).cuda()].any())
+    q = banded(8, 500, 500, 20, 20, 128)  # fp32 B: the CUDA-core window kernel runs
+    check(q, kernel="window_tc")
+
+
+def test_tc_deterministic():
+    p = banded(9, 2000, 2000, 32, 31, 256, b_dtype="bf16")
+    C1, _ = H.run(p, kernel="window_tc")
+    C2, _ = H.run(p, kernel="window_tc")
     assert torch.equal(C1, C2)
