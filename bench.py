@@ -110,18 +110,17 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# The sources that define each timed kernel (what a traffic record depends on).
+# The device sources that define each timed kernel (what a traffic record depends on).
 KERNEL_SOURCES = {
     "row": ["spmm_row.cuh", "spmm_row_f32.cu", "spmm_row_bf16.cu"],
-    "balanced": ["spmm_balanced.cuh", "spmm_balanced_f32.cu", "spmm_balanced_bf16.cu", "spmm_sddmm.cuh",
-                 "spmm_plan.cu"],
+    "balanced": ["spmm_balanced.cuh", "spmm_balanced_f32.cu", "spmm_balanced_bf16.cu", "spmm_sddmm.cuh"],
     "window": ["spmm_window.cuh", "spmm_window.cu"],
     "window_tc": ["spmm_tc_window.cuh", "spmm_tc_window.cu"],
     "smalln": ["spmm_rowgroup.cuh", "spmm_rowgroup.cu"],
     "sddmm": ["spmm_sddmm.cuh", "spmm_sddmm_f32.cu"],
-    "fusedmm": ["spmm_balanced.cuh", "spmm_fusedmm_f32.cu", "spmm_sddmm.cuh", "spmm_plan.cu"],
+    "fusedmm": ["spmm_balanced.cuh", "spmm_fusedmm_f32.cu", "spmm_sddmm.cuh"],
 }
-COMMON_SOURCES = ["spmm_device.cuh", "spmm_internal.h", "spmm_api.cu"]
+COMMON_SOURCES = ["spmm_device.cuh"]
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -360,6 +359,8 @@ def gpu_arm(args, p, cfg, ws, rank, local):
                               items_per_cta=args.items_per_cta)
     if args.group_lanes:
         spmm.spmm_plan_set_group_lanes(plan, args.group_lanes)
+    if args.column_tile:
+        spmm.spmm_plan_set_column_tile(plan, args.column_tile)
     torch.cuda.synchronize()
     plan_ms = (time.perf_counter() - t0) * 1e3
     info = plan.info()
@@ -527,6 +528,7 @@ def main(argv=None):
     ap.add_argument("--n", type=int, default=0, help="dense width: redraw B with this many columns")
     ap.add_argument("--semiring", default="sum,mul", help="(+),(x): sum|min|max , mul|add (SpMM only)")
     ap.add_argument("--group-lanes", type=int, default=0, help="lanes per row of a smalln plan")
+    ap.add_argument("--column-tile", type=int, default=0, help="N-slicing: cap the column tile (row/balanced)")
     ap.add_argument("--items-per-cta", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -62,7 +62,8 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
   const bool vector_ok = plan->N % (bf16 ? 8 : 4) == 0 && aligned16(B) && aligned16(C);
   const bool row_family = plan->kernel == SPMM_KERNEL_ROW || plan->kernel == SPMM_KERNEL_WINDOW ||
                           plan->kernel == SPMM_KERNEL_SMALLN || plan->kernel == SPMM_KERNEL_WINDOW_TC;
-  const Shape s = row_family ? choose_shape(plan->N, bf16, vector_ok) : choose_shape_balanced(plan->N, bf16, vector_ok);
+  const Shape s = cap_tile(row_family ? choose_shape(plan->N, bf16, vector_ok)
+                                      : choose_shape_balanced(plan->N, bf16, vector_ok), plan->column_tile);
   const bool window_family = plan->kernel == SPMM_KERNEL_WINDOW || plan->kernel == SPMM_KERNEL_WINDOW_TC;
   const bool window = window_family && s.G == 32 && s.nch == 1 && s.vec == (bf16 ? 8 : 4);
   const bool window_tc = plan->kernel == SPMM_KERNEL_WINDOW_TC && bf16 && plan->N % 16 == 0 && plan->N <= 256 &&
@@ -159,7 +160,7 @@ spmm_status semiring(spmm_plan_t plan, int32_t K, const int32_t* colind, const f
   L.vals = vals;
   L.B = B;
   L.C = C;
-  cudaError_t e = launch_semiring_f32(L, choose_shape_balanced(plan->N, false, vector_ok), sr);
+  cudaError_t e = launch_semiring_f32(L, cap_tile(choose_shape_balanced(plan->N, false, vector_ok), plan->column_tile), sr);
   if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
   if (e == cudaSuccess) e = launch_fixup(L, sr);
   return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;

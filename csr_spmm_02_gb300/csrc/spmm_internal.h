@@ -38,6 +38,7 @@ struct spmm_plan_s {
   int32_t items_per_cta = 0;  // balanced only
   int32_t num_ctas = 0;       // balanced only
   int32_t group_lanes = 0;    // SMALLN only: lanes sharing a row
+  int32_t column_tile = 0;    // N-slicing cap of the row and balanced kernels (0: none)
   int device = 0;
   bool stream_ordered = false;  // workspace from cudaMallocAsync (one-call form)
   // device workspace (one allocation, carved up)
@@ -82,13 +83,16 @@ Shape choose_shape(int32_t N, bool bf16, bool vector_ok, int chunks_f32);
 inline Shape choose_shape(int32_t N, bool bf16, bool vector_ok) {
   return choose_shape(N, bf16, vector_ok, SPMM_LANE_CHUNKS);
 }
-#ifndef SPMM_BAL_MAX_TW
-#define SPMM_BAL_MAX_TW 0
-#endif
 inline Shape choose_shape_balanced(int32_t N, bool bf16, bool vector_ok) {
-  Shape s = choose_shape(N, bf16, vector_ok, SPMM_BAL_CHUNKS);
-  if (SPMM_BAL_MAX_TW > 0)
-    while (s.G > 1 && s.tile_width() > SPMM_BAL_MAX_TW) s.G >>= 1;
+  return choose_shape(N, bf16, vector_ok, SPMM_BAL_CHUNKS);
+}
+
+// N-slicing: narrow the column tile (fewer lanes per group) until it spans at
+// most `cap` columns (0: no cap).  Column tiles run as grid.y, and CTAs of
+// tile 0 are scheduled before those of tile 1, so each tile's slice of B is
+// what the caches hold at a time.
+inline Shape cap_tile(Shape s, int32_t cap) {
+  while (cap > 0 && s.G > 1 && s.tile_width() > cap) s.G >>= 1;
   return s;
 }
 

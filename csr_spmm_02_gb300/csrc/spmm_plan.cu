@@ -265,6 +265,14 @@ spmm_status spmm_plan_get_info(spmm_plan_t plan, spmm_plan_info* info) {
   info->num_ctas = plan->num_ctas;
   info->workspace_bytes = plan->workspace_bytes;
   info->group_lanes = plan->group_lanes;
+  info->column_tile = plan->column_tile;
+  return SPMM_OK;
+}
+
+spmm_status spmm_plan_set_column_tile(spmm_plan_t plan, int32_t columns) {
+  if (!plan) return SPMM_ERR_PLAN_MISMATCH;
+  if (columns < 0) return SPMM_ERR_INVALID_ARG;
+  plan->column_tile = columns;
   return SPMM_OK;
 }
 

@@ -38,7 +38,7 @@ EXPORTS = ["spmm_csr_plan", "spmm_csr_plan_ex", "spmm_plan_get_info", "spmm_plan
            "spmm_csr_f32_exec", "spmm_csr_bf16f32_exec", "spmm_csr_f32", "spmm_csr_bf16f32",
            "spmm_csr_validate", "spmm_plan_check_device", "spmm_plan_set_split_event",
            "spmm_csr_f32_noalloc", "spmm_csr_sddmm_f32", "spmm_csr_fusedmm_f32", "spmm_csr_semiring_f32_exec",
-           "spmm_plan_set_group_lanes", "spmm_status_string"]
+           "spmm_plan_set_group_lanes", "spmm_plan_set_column_tile", "spmm_status_string"]
 
 
 class SpmmError(RuntimeError):
@@ -51,7 +51,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("M", ctypes.c_int32), ("nnz", ctypes.c_int64),
                 ("N", ctypes.c_int32), ("max_row_nnz", ctypes.c_int32), ("empty_rows", ctypes.c_int32),
                 ("items_per_cta", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64), ("group_lanes", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_int64), ("group_lanes", ctypes.c_int32),
+                ("column_tile", ctypes.c_int32)]
 
 
 _lib = None
@@ -88,6 +89,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "spmm_csr_fusedmm_f32": [vp, i32, vp, vp, vp, vp, vp, vp],
         "spmm_csr_semiring_f32_exec": [vp, i32, vp, vp, vp, vp, i32, i32, vp],
         "spmm_plan_set_group_lanes": [vp, i32],
+        "spmm_plan_set_column_tile": [vp, i32],
         "spmm_status_string": [ctypes.c_int],
     }
     for name, args in sig.items():
@@ -202,6 +204,11 @@ def spmm_csr_sddmm_f32(plan: Plan, K, colind, C, B, out, stream=None):
 def spmm_plan_set_group_lanes(plan: Plan, lanes: int):
     """Lanes (2, 4, 8, 16, 32) that share a row in a SMALLN plan."""
     _check(load().spmm_plan_set_group_lanes(plan.handle, lanes), "spmm_plan_set_group_lanes")
+
+
+def spmm_plan_set_column_tile(plan: Plan, columns: int):
+    """Cap the row/balanced kernels' column tile at `columns` (N-slicing; 0: no cap)."""
+    _check(load().spmm_plan_set_column_tile(plan.handle, columns), "spmm_plan_set_column_tile")
 
 
 ADD_OPS = {"sum": 0, "min": 1, "max": 2}

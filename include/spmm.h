@@ -121,6 +121,7 @@ typedef struct {
   int32_t num_ctas;        /* balanced: number of merge-path ranges (CTAs) */
   int64_t workspace_bytes; /* device bytes the plan owns */
   int32_t group_lanes;     /* SMALLN: lanes r that share a row (2..32) */
+  int32_t column_tile;     /* N-slicing cap set by spmm_plan_set_column_tile (0: none) */
 } spmm_plan_info;
 
 /*
@@ -149,6 +150,17 @@ SPMM_API spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t 
 /* Set the lanes r (2, 4, 8, 16 or 32) that share a row in the SMALLN kernel;
  * SPMM_ERR_INVALID_ARG for another value or a plan of another kernel. */
 SPMM_API spmm_status spmm_plan_set_group_lanes(spmm_plan_t plan, int32_t lanes);
+
+/*
+ * N-slicing (survey of L2-level chunking; the kkmem page's chunking moved from
+ * host/HBM to L2/HBM): cap the column tile of the row and balanced kernels at
+ * `columns` (0 removes the cap), so that each tile's slice of B (K x tile
+ * columns) is what L2 holds at a time; the tiles run in order.  The plan's
+ * own choice is one tile: on the measured workloads narrower tiles were
+ * slower (each repeats every nonzero's bookkeeping).  The window and
+ * small-N kernels keep their own tiles.  SPMM_ERR_INVALID_ARG if columns < 0.
+ */
+SPMM_API spmm_status spmm_plan_set_column_tile(spmm_plan_t plan, int32_t columns);
 
 /* Copy the plan's decisions into *info (host memory).  Every plan also holds
  * the merge-path partition used by the balanced SpMM, SDDMM and FusedMM. */

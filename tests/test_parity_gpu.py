@@ -190,3 +190,20 @@ def test_side_stream():
         C, _ = H.run(p, kernel="balanced", arrays=a, C=C, stream=s)
     C_ref, S = H.reference(p)
     H.assert_within(C, C_ref, S, "f32", "side stream")
+
+
+@pytest.mark.parametrize("kernel", ["row", "balanced"])
+@pytest.mark.parametrize("b_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cap", [8, 32, 64])
+def test_column_tile_cap(kernel, b_dtype, cap):
+    """N-slicing: the same results with the column tile capped (several tiles in grid.y)."""
+    p = mixed(7 + cap, N=256, b_dtype=b_dtype)
+    a = H.device_arrays(p)
+    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N, kernel=kernel, items_per_cta=256)
+    spmm.spmm_plan_set_column_tile(plan, cap)
+    assert plan.info()["column_tile"] == cap
+    C, _ = H.run(p, arrays=a, plan=plan)
+    C_ref, S = H.reference(p)
+    H.assert_within(C, C_ref, S, b_dtype, f"{kernel}/{b_dtype}/cap={cap}")
+    with pytest.raises(spmm.SpmmError):
+        spmm.spmm_plan_set_column_tile(plan, -1)
