@@ -95,3 +95,13 @@ def test_random_csr_options():
     p = gen.random_csr(rng, 50, 20, 7, duplicates=True, sort_cols=False, integer=True, b_dtype="bf16")
     _check_csr(p, distinct_sorted=False)
     assert p.B.dtype == np.uint16
+
+
+@pytest.mark.parametrize("name,prefixes", [
+    ("uniform1k", ("4f124b61969c4f0f", "a59d395f092f2e5a", "2ca73052517df28f", "e9bad8adf6e3237f")),
+    ("uniform64k", ("f8675858ad786334", "c9b7206181dbc2ac", "67d8484d3eee11a5", "9436afcbe8c5a585")),
+])
+def test_workload_digests_are_stable(name, prefixes):
+    """The generator reproduces the arrays recorded with the measurements (rowptr, colind, vals, B)."""
+    d = gen.make_workload(name).digest()
+    assert tuple(d[k][:16] for k in ("rowptr", "colind", "vals", "B")) == prefixes
