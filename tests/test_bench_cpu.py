@@ -26,7 +26,7 @@ def test_dense_operands_are_seeded_fp32():
     C2, B2, D2 = bench.op_dense_inputs(p, "fusedmm")
     assert C1.dtype == np.float32 and C1.shape == (p.M, p.N) and D1.shape == (p.K, p.N)
     assert np.array_equal(C1, C2) and np.array_equal(D1, D2) and np.array_equal(B1, p.B)
-    q = gen.make_workload("banded")
+    q = gen.random_csr(np.random.default_rng(1), 50, 40, 24, b_dtype="bf16")
     _, Bq, _ = bench.op_dense_inputs(q, "sddmm")  # bf16 B widened exactly
     assert Bq.dtype == np.float32
     assert np.array_equal((q.B.astype(np.uint32) << 16).view(np.float32), Bq)

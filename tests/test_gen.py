@@ -30,13 +30,23 @@ def test_uniform_workloads(name, nnz, cbytes):
 
 
 def test_banded_workload():
-    p = gen.make_workload("banded")
-    _check_csr(p)
-    assert p.nnz == 16776192 and p.compulsory_bytes() == 537911300
-    assert p.B.dtype == np.uint16 and p.B.shape == (262144, 256)
-    for i in (0, 1, 31, 32, 100000, 262112, 262143):
-        cols = p.colind[p.rowptr[i]:p.rowptr[i + 1]]
-        assert np.array_equal(cols, np.arange(max(0, i - 32), min(262143, i + 31) + 1))
+    """The banded structure (row i: columns i-32 .. i+31, clipped) on a smaller matrix with the
+    same band, and the full-size nnz / compulsory bytes in closed form: every row holds 64
+    columns except the 32 first and 31 last rows, clipped by 32-i and i-(K-32) columns."""
+    spec = gen.WORKLOADS["banded"]
+    M, below, above, N = spec["M"], spec["below"], spec["above"], spec["N"]
+    clipped = sum(below - i for i in range(below)) + sum(above - i for i in range(above))
+    nnz_full = M * (below + above + 1) - clipped
+    assert nnz_full == 16776192
+    assert 4 * (M + 1) + 8 * nnz_full + M * N * 2 + 4 * M * N == 537911300  # compulsory bytes, bf16 B
+    m = 5000
+    rowptr, colind = gen.banded_structure(m, m, below, above)
+    assert int(rowptr[-1]) == m * (below + above + 1) - clipped and len(colind) == int(rowptr[-1])
+    for i in (0, 1, 31, 32, 2500, m - 32, m - 1):
+        cols = colind[rowptr[i]:rowptr[i + 1]]
+        assert np.array_equal(cols, np.arange(max(0, i - below), min(m - 1, i + above) + 1))
+    small = gen.random_csr(np.random.default_rng(0), 40, 30, 16, b_dtype="bf16")
+    assert small.B.dtype == np.uint16 and small.B.shape == (30, 16)
 
 
 def test_bf16_rounding_matches_torch():
