@@ -32,6 +32,9 @@
 #ifndef SPMM_SDDMM_LOADS
 #define SPMM_SDDMM_LOADS 4  // nonzeros whose operand rows a lane has in flight (per chunk)
 #endif
+#ifndef SPMM_SDDMM_LOADS_WIDE
+#define SPMM_SDDMM_LOADS_WIDE 2  // the same for 32-lane groups (each lane already keeps 32 partial sums)
+#endif
 
 namespace spmm {
 
@@ -134,7 +137,8 @@ __global__ void __launch_bounds__(kThreads)
                       const int2* __restrict__ part, int32_t T, int* __restrict__ err) {
   constexpr int S = 32 / G;                     // nonzeros per warp step
   constexpr int W = kThreads / 32;
-  constexpr int U = SPMM_SDDMM_LOADS / NCH > 0 ? SPMM_SDDMM_LOADS / NCH : 1;  // steps per load batch
+  constexpr int kLoads = G >= 32 ? SPMM_SDDMM_LOADS_WIDE : SPMM_SDDMM_LOADS;
+  constexpr int U = kLoads / NCH > 0 ? kLoads / NCH : 1;  // steps per load batch
   constexpr int R = G > U ? G : U;              // steps per warp iteration
   constexpr int NPI = R * S;                    // nonzeros per warp iteration
   static_assert(R % U == 0 && R % G == 0, "powers of two");
