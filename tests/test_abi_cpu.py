@@ -68,3 +68,38 @@ def test_binding_refuses_cpu_tensors(lib):
     import torch
     with pytest.raises(ValueError):
         spmm.spmm_csr_plan(torch.zeros(5, dtype=torch.int32), 4, 0, 8)
+
+
+C_USER = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "spmm.h"
+
+/* A C99 user of the library: argument errors come back as status codes
+   before any CUDA call, so this runs on a machine without a GPU. */
+int main(void) {
+  spmm_plan_t plan = (spmm_plan_t)0;
+  int bad = 0;
+  if (spmm_csr_plan(NULL, 10, 5, 4, NULL, &plan) != SPMM_ERR_INVALID_ARG) bad |= 1;
+  if (plan != NULL) bad |= 2;
+  if (spmm_csr_plan_ex(NULL, 0, 0, 4, 99, 0, NULL, &plan) != SPMM_ERR_INVALID_ARG) bad |= 4;
+  if (spmm_csr_f32(-1, 1, 1, NULL, NULL, NULL, NULL, NULL, NULL) != SPMM_ERR_INVALID_ARG) bad |= 8;
+  if (spmm_csr_f32_exec(NULL, 1, NULL, NULL, NULL, NULL, NULL) != SPMM_ERR_PLAN_MISMATCH) bad |= 16;
+  if (spmm_plan_set_column_tile(NULL, 8) != SPMM_ERR_PLAN_MISMATCH) bad |= 32;
+  printf("%s %d\n", spmm_status_string(SPMM_ERR_INVALID_CSR), bad);
+  return bad;
+}
+"""
+
+
+def test_header_is_c99_and_a_c_program_links(lib, tmp_path):
+    """include/spmm.h compiles as strict C99 and a C program links the library."""
+    import subprocess
+    src = tmp_path / "user.c"
+    src.write_text(C_USER)
+    exe = tmp_path / "user"
+    libpath = spmm.library_path()
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
+                    str(src), "-o", str(exe), libpath, f"-Wl,-rpath,{os.path.dirname(libpath)}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.split() == ["SPMM_ERR_INVALID_CSR", "0"], (out.returncode, out.stdout)
