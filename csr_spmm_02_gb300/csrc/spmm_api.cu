@@ -180,7 +180,15 @@ spmm_status fusedmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const fl
   L.colind = colind;
   L.B = D;  // gathered and accumulated
   L.C = E;
-  cudaError_t e = launch_fusedmm_f32(L, choose_shape_balanced(plan->N, false, vector_ok), Cd, B);
+  // Every column tile recomputes the dot products over all N columns, so wide
+  // rows take one tile of up to 512 columns (two or four chunks per lane).
+  Shape s = choose_shape_balanced(plan->N, false, vector_ok);
+  if (vector_ok && s.G == 32 && plan->N > s.tile_width()) {
+    int nch = 1;
+    while (nch < 4 && 32 * 4 * nch < plan->N) nch <<= 1;
+    s = Shape{4, 32, nch};
+  }
+  cudaError_t e = launch_fusedmm_f32(L, s, Cd, B);
   if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
   if (e == cudaSuccess) e = launch_fixup(L);
   return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;

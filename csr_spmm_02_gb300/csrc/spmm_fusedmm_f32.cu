@@ -8,6 +8,7 @@ cudaError_t launch_fusedmm_f32(const Launch& L, Shape s, const float* Cd, const 
   if (s.vec == V && s.G == GG && s.nch == NC) return launch_balanced_t<float, V, GG, NC, true>(L, Cd, Bd);
   SPMM_VECTOR_SHAPES(X, 4, SPMM_BAL_CHUNKS)
   SPMM_SCALAR_SHAPES(X)
+  X(4, 32, 2) X(4, 32, 4)  // one tile for wide rows
 #undef X
   return cudaErrorInvalidConfiguration;
 }
