@@ -137,7 +137,15 @@ spmm_status sddmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const floa
   L.K = K;
   L.colind = colind;
   L.B = B;
-  const cudaError_t e = launch_sddmm_f32(L, choose_shape_balanced(plan->N, false, vector_ok), Cd, out);
+  // Rows wider than one 128-column tile: two or four chunks per lane, so the
+  // whole dot product comes from batched loads.
+  Shape s = choose_shape_balanced(plan->N, false, vector_ok);
+  if (vector_ok && s.G == 32 && plan->N > s.tile_width()) {
+    int nch = 1;
+    while (nch < 4 && 32 * 4 * nch < plan->N) nch <<= 1;
+    s = Shape{4, 32, nch};
+  }
+  const cudaError_t e = launch_sddmm_f32(L, s, Cd, out);
   return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
 }
 
