@@ -5,8 +5,7 @@
 #include "spmm_internal.h"
 
 spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N, int32_t kernel,
-                           int32_t items_per_cta, cudaStream_t stream, bool stream_ordered,
-                           spmm_plan_t* plan_out);
+                           int32_t items_per_cta, cudaStream_t stream, bool one_call, spmm_plan_t* plan_out);
 void spmm_free_plan(spmm_plan_t plan, cudaStream_t stream);
 
 namespace spmm {
@@ -208,14 +207,9 @@ spmm_status one_call(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, con
   if (M == 0 || N == 0) return SPMM_OK;
   if (!rowptr) return SPMM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // nnz = rowptr[M] is needed on the host to size the plan.
-  int32_t nnz = 0;
-  if (cudaMemcpyAsync(&nnz, rowptr + M, sizeof nnz, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return SPMM_ERR_CUDA;
-  if (nnz < 0) return SPMM_ERR_INVALID_CSR;
+  // nnz = rowptr[M] comes back with the row statistics (one synchronisation).
   spmm_plan_t plan = nullptr;
-  spmm_status st = spmm_make_plan(rowptr, M, nnz, N, SPMM_KERNEL_AUTO, 0, s, true, &plan);
+  spmm_status st = spmm_make_plan(rowptr, M, -1, N, SPMM_KERNEL_AUTO, 0, s, true, &plan);
   if (st != SPMM_OK) return st;
   st = exec(plan, K, colind, vals, B, bf16, C, s);
   spmm_free_plan(plan, s);

@@ -2,6 +2,7 @@
 // CSR validation and the deterministic fixup of rows split across CTAs.
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 #include <new>
 
 #include "spmm_device.cuh"
@@ -9,9 +10,10 @@
 
 namespace spmm {
 
-// stats[0] = longest row, stats[1] = number of empty rows.
+// stats[0] = longest row, stats[1] = number of empty rows, stats[2] = rowptr[M].
 __global__ void __launch_bounds__(kThreads) row_stats_kernel(const int32_t* __restrict__ rowptr, int32_t M,
                                                              int* __restrict__ stats) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) stats[2] = __ldg(rowptr + M);
   int longest = 0, empty = 0;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < M; i += int64_t(gridDim.x) * blockDim.x) {
     const int len = __ldg(rowptr + i + 1) - __ldg(rowptr + i);
@@ -119,8 +121,42 @@ using namespace spmm;
 
 namespace {
 
+// The one-call forms allocate from a pool of their own on each device, with
+// the release threshold raised so that freed blocks stay reserved for the
+// next call.  (The device's default pool returns its memory to the system at
+// every synchronisation, and mapping it again costs about 0.1 ms per call.)
+std::mutex g_pool_mutex;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+cudaError_t one_call_pool(cudaMemPool_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_pool_mutex);
+  if (!g_pool[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return e;
+    uint64_t keep = UINT64_MAX;
+    if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return e;
+    }
+    g_pool[dev] = pool;
+  }
+  *out = g_pool[dev];
+  return cudaSuccess;
+}
+
 cudaError_t dev_alloc(void** p, size_t bytes, bool stream_ordered, cudaStream_t s) {
-  return stream_ordered ? cudaMallocAsync(p, bytes, s) : cudaMalloc(p, bytes);
+  if (!stream_ordered) return cudaMalloc(p, bytes);
+  cudaMemPool_t pool = nullptr;
+  const cudaError_t e = one_call_pool(&pool);
+  return e == cudaSuccess ? cudaMallocFromPoolAsync(p, bytes, pool, s) : e;
 }
 void dev_free(void* p, bool stream_ordered, cudaStream_t s) {
   if (!p) return;
@@ -135,12 +171,14 @@ unsigned stats_grid(int32_t M) {
 }  // namespace
 
 // Plan construction shared by spmm_csr_plan(_ex) and the one-call forms.
+// one_call: nnz is read from rowptr[M] along with the row statistics (the
+// caller passes -1), the workspace comes from the one-call pool, and the
+// merge-path partition is built only when the chosen kernel uses it.
 spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N, int32_t kernel,
-                           int32_t items_per_cta, cudaStream_t stream, bool stream_ordered,
-                           spmm_plan_t* plan_out) {
+                           int32_t items_per_cta, cudaStream_t stream, bool one_call, spmm_plan_t* plan_out) {
   if (!plan_out) return SPMM_ERR_INVALID_ARG;
   *plan_out = nullptr;
-  if (M < 0 || N < 0 || nnz < 0) return SPMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || (nnz < 0 && !one_call)) return SPMM_ERR_INVALID_ARG;
   if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
   if (M > 0 && !rowptr) return SPMM_ERR_INVALID_ARG;
   if (kernel < SPMM_KERNEL_AUTO || kernel > SPMM_KERNEL_WINDOW_TC) return SPMM_ERR_INVALID_ARG;
@@ -150,10 +188,10 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   spmm_plan_s* plan = new (std::nothrow) spmm_plan_s();
   if (!plan) return SPMM_ERR_CUDA;
   plan->M = M;
-  plan->nnz = nnz;
+  plan->nnz = std::max<int64_t>(nnz, 0);
   plan->N = N;
   plan->rowptr = rowptr;
-  plan->stream_ordered = stream_ordered;
+  plan->stream_ordered = one_call;
   plan->kernel = kernel == SPMM_KERNEL_AUTO ? SPMM_KERNEL_ROW : kernel;
   if (cudaGetDevice(&plan->device) != cudaSuccess) {
     delete plan;
@@ -164,28 +202,30 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
     return SPMM_OK;
   }
 
-  auto fail = [&](cudaError_t) {
-    dev_free(plan->workspace, stream_ordered, stream);
-    dev_free(plan->err, stream_ordered, stream);
+  auto fail = [&](spmm_status st) {
+    dev_free(plan->workspace, one_call, stream);
+    dev_free(plan->err, one_call, stream);
     delete plan;
-    return SPMM_ERR_CUDA;
+    return st;
   };
 
   // error word + statistics (16 bytes)
   void* small = nullptr;
-  cudaError_t e = dev_alloc(&small, 16, stream_ordered, stream);
-  if (e != cudaSuccess) return fail(e);
+  cudaError_t e = dev_alloc(&small, 16, one_call, stream);
+  if (e != cudaSuccess) return fail(SPMM_ERR_CUDA);
   plan->err = static_cast<int*>(small);
   plan->stats = plan->err + 1;
-  if ((e = cudaMemsetAsync(small, 0, 16, stream)) != cudaSuccess) return fail(e);
+  if ((e = cudaMemsetAsync(small, 0, 16, stream)) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   row_stats_kernel<<<stats_grid(M), kThreads, 0, stream>>>(rowptr, M, plan->stats);
-  if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
-  int host_stats[2] = {0, 0};
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail(SPMM_ERR_CUDA);
+  int host_stats[3] = {0, 0, 0};
   if ((e = cudaMemcpyAsync(host_stats, plan->stats, sizeof host_stats, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
-    return fail(e);
-  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return fail(e);
+    return fail(SPMM_ERR_CUDA);
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   plan->max_row_nnz = host_stats[0];
   plan->empty_rows = host_stats[1];
+  if (host_stats[2] < 0 || (nnz >= 0 && host_stats[2] != nnz)) return fail(SPMM_ERR_INVALID_CSR);
+  nnz = plan->nnz = host_stats[2];
 
   if (kernel == SPMM_KERNEL_AUTO) {
     // Short, even rows: one group per row keeps all lanes busy with no
@@ -209,24 +249,26 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
     plan->group_lanes = r;
   }
 
-  {  // merge-path partition and carry rows: used by the balanced SpMM, SDDMM and FusedMM
+  // merge-path partition and carry rows: used by the balanced SpMM, SDDMM and
+  // FusedMM (a one-call SpMM on another kernel needs neither)
+  if (!one_call || plan->kernel == SPMM_KERNEL_BALANCED) {
     const int T = items_per_cta ? items_per_cta : kDefaultItemsPerCta;
     const int64_t total = int64_t(M) + nnz;
     const int64_t P = (total + T - 1) / T;
-    if (P > INT32_MAX - 1) return fail(cudaErrorInvalidValue);
+    if (P > INT32_MAX - 1) return fail(SPMM_ERR_UNSUPPORTED);
     plan->items_per_cta = T;
     plan->num_ctas = int32_t(P);
     const size_t part_bytes = (size_t(P) + 1) * sizeof(int2);
     const size_t part_padded = (part_bytes + 255) & ~size_t(255);
     const size_t carry_bytes = size_t(P) * 2 * size_t(N) * sizeof(float);
     plan->workspace_bytes = int64_t(part_padded + carry_bytes);
-    if ((e = dev_alloc(&plan->workspace, part_padded + carry_bytes, stream_ordered, stream)) != cudaSuccess)
-      return fail(e);
+    if ((e = dev_alloc(&plan->workspace, part_padded + carry_bytes, one_call, stream)) != cudaSuccess)
+      return fail(SPMM_ERR_CUDA);
     plan->part = static_cast<int2*>(plan->workspace);
     plan->carry = reinterpret_cast<float*>(static_cast<char*>(plan->workspace) + part_padded);
     const unsigned grid = unsigned((P + 1 + kThreads - 1) / kThreads);
     merge_path_partition_kernel<<<grid, kThreads, 0, stream>>>(rowptr, M, nnz, T, int32_t(P), plan->part);
-    if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   }
   plan->workspace_bytes += 16;
   *plan_out = plan;
@@ -309,7 +351,7 @@ spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int3
   if (!rowptr || (nnz > 0 && !colind)) return SPMM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* flag = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&flag), sizeof(int), s) != cudaSuccess) return SPMM_ERR_CUDA;
+  if (dev_alloc(reinterpret_cast<void**>(&flag), sizeof(int), true, s) != cudaSuccess) return SPMM_ERR_CUDA;
   int host = 0;
   cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(int), s);
   if (e == cudaSuccess) {
@@ -319,10 +361,17 @@ spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int3
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = cudaMemcpyAsync(&host, flag, sizeof(int), cudaMemcpyDeviceToHost, s);
-  cudaFreeAsync(flag, s);
+  dev_free(flag, true, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return SPMM_ERR_CUDA;
   return host ? SPMM_ERR_INVALID_CSR : SPMM_OK;
+}
+
+spmm_status spmm_pool_release(void) {
+  std::lock_guard<std::mutex> lock(g_pool_mutex);
+  for (int d = 0; d < kMaxDevices; ++d)
+    if (g_pool[d] && cudaMemPoolTrimTo(g_pool[d], 0) != cudaSuccess) return SPMM_ERR_CUDA;
+  return SPMM_OK;
 }
 
 }  // extern "C"

@@ -38,7 +38,8 @@ EXPORTS = ["spmm_csr_plan", "spmm_csr_plan_ex", "spmm_plan_get_info", "spmm_plan
            "spmm_csr_f32_exec", "spmm_csr_bf16f32_exec", "spmm_csr_f32", "spmm_csr_bf16f32",
            "spmm_csr_validate", "spmm_plan_check_device", "spmm_plan_set_split_event",
            "spmm_csr_f32_noalloc", "spmm_csr_sddmm_f32", "spmm_csr_fusedmm_f32", "spmm_csr_semiring_f32_exec",
-           "spmm_plan_set_group_lanes", "spmm_plan_set_column_tile", "spmm_status_string"]
+           "spmm_plan_set_group_lanes", "spmm_plan_set_column_tile", "spmm_pool_release",
+           "spmm_status_string"]
 
 
 class SpmmError(RuntimeError):
@@ -90,6 +91,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "spmm_csr_semiring_f32_exec": [vp, i32, vp, vp, vp, vp, i32, i32, vp],
         "spmm_plan_set_group_lanes": [vp, i32],
         "spmm_plan_set_column_tile": [vp, i32],
+        "spmm_pool_release": [],
         "spmm_status_string": [ctypes.c_int],
     }
     for name, args in sig.items():
@@ -241,6 +243,11 @@ def spmm_csr_f32_noalloc(M, K, N, nnz, rowptr, colind, vals, B, C, stream=None):
                                        _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True), _ptr(C, _F32, "C"),
                                        _stream(stream)), "spmm_csr_f32_noalloc")
     return C
+
+
+def spmm_pool_release() -> None:
+    """Hand back the device memory the one-call forms' pools keep between calls."""
+    _check(load().spmm_pool_release(), "spmm_pool_release")
 
 
 def spmm_csr_validate(rowptr, colind, M, K, nnz, stream=None) -> int:

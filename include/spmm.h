@@ -111,7 +111,7 @@ typedef struct spmm_plan_s* spmm_plan_t;
 
 /* What a plan decided (host copy, filled by spmm_plan_get_info). */
 typedef struct {
-  int32_t kernel;          /* SPMM_KERNEL_ROW, _BALANCED or _WINDOW */
+  int32_t kernel;          /* the spmm_kernel value exec runs (never SPMM_KERNEL_AUTO) */
   int32_t M;
   int64_t nnz;
   int32_t N;
@@ -127,13 +127,14 @@ typedef struct {
 /*
  * Build a plan for A's row structure (nnz-balanced row partitioning).
  * Reads rowptr (device, M+1 entries) on `stream`: one small kernel computes
- * the row-length statistics, which are copied to the host (this call
- * synchronises `stream` once); for the balanced kernel a second kernel
- * computes the merge-path partition (a binary search per range over the
- * merged sequence of row ends and nonzeros -- the even nnz split the Sgap
- * page's related work attributes to Yang et al., and the element-balanced
- * EB scheme of its DA-SpMM design space).  The plan's workspace is
- * allocated with cudaMalloc.  *plan_out receives the plan (NULL on error).
+ * the row-length statistics and reads rowptr[M], which are copied to the
+ * host (this call synchronises `stream` once); a second kernel computes the
+ * merge-path partition (a binary search per range over the merged sequence
+ * of row ends and nonzeros -- the even nnz split the Sgap page's related
+ * work attributes to Yang et al., and the element-balanced EB scheme of its
+ * DA-SpMM design space).  nnz must equal rowptr[M]: SPMM_ERR_INVALID_CSR
+ * otherwise.  The plan's workspace is allocated with cudaMalloc.  *plan_out
+ * receives the plan (NULL on error).
  */
 SPMM_API spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
                           void* stream, spmm_plan_t* plan_out);
@@ -232,10 +233,15 @@ SPMM_API spmm_status spmm_csr_fusedmm_f32(spmm_plan_t plan, int32_t K, const int
                                           const float* B, const float* D, float* E, void* stream);
 
 /*
- * One-call form: plans, multiplies and frees on `stream`.  Plan workspace is
- * stream-ordered (cudaMallocAsync / cudaFreeAsync); the plan's statistics
- * copy synchronises `stream` once.  For repeated products with the same A,
- * build a plan once and call the _exec form.
+ * One-call form: plans, multiplies and frees on `stream`.  nnz is read from
+ * rowptr[M] with the plan's statistics (one copy, which synchronises `stream`
+ * once; SPMM_ERR_INVALID_CSR if it is negative).  The plan's workspace comes
+ * stream-ordered (cudaMallocFromPoolAsync / cudaFreeAsync) from a pool the
+ * library creates on each device at its first one-call use; the pool keeps
+ * freed blocks reserved for later calls (spmm_pool_release hands them back),
+ * so repeated calls map no new memory.  The merge-path partition is built
+ * only when the chosen kernel is the balanced one.  For repeated products
+ * with the same A, build a plan once and call the _exec form.
  */
 SPMM_API spmm_status spmm_csr_f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
                          const int32_t* colind, const float* vals, const float* B, float* C,
@@ -250,7 +256,7 @@ SPMM_API spmm_status spmm_csr_bf16f32(int32_t M, int32_t K, int32_t N, const int
  * Check a CSR structure on the device: rowptr[0] = 0, rowptr non-decreasing,
  * rowptr[M] = nnz, every colind in [0, K).  Synchronous (waits for
  * `stream`).  Returns SPMM_OK or SPMM_ERR_INVALID_CSR.  Uses a 4-byte
- * stream-ordered device allocation.
+ * stream-ordered device allocation from the one-call pool.
  */
 SPMM_API spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int32_t M,
                               int32_t K, int64_t nnz, void* stream);
@@ -297,6 +303,15 @@ SPMM_API spmm_status spmm_csr_f32_noalloc(int32_t M, int32_t K, int32_t N, int64
  * caller owns the event and keeps it alive while it is set.
  */
 SPMM_API spmm_status spmm_plan_set_split_event(spmm_plan_t plan, void* event);
+
+/*
+ * Return to the system the device memory that the one-call forms' pools
+ * (one per device, see spmm_csr_f32) keep reserved between calls.  Blocks
+ * still in use, or freed on a stream that has not reached the free yet, stay
+ * with the pool: synchronise the streams that ran one-call forms first.
+ * Safe to call at any time, from any thread; SPMM_ERR_CUDA if a trim fails.
+ */
+SPMM_API spmm_status spmm_pool_release(void);
 
 /* Static, human-readable name of a status code. */
 SPMM_API const char* spmm_status_string(spmm_status status);
