@@ -181,6 +181,32 @@ def test_one_call_form_matches_plan_exec(b_dtype):
         assert plan.info()["kernel"] == ("row" if uniform else "balanced")
 
 
+def test_one_call_pool_reuse_and_release():
+    """Repeated one-call products reuse the pool's blocks; after a release the next call maps new
+    memory and gives the same bits.  A negative rowptr[M] is rejected as an invalid CSR."""
+    p = mixed(5, N=64)
+    a = H.device_arrays(p)
+    C_ref, S = H.reference(p)
+    outs = []
+    for i in range(4):
+        C = torch.full((p.M, p.N), float("nan"), device="cuda")
+        spmm.spmm_csr_f32(p.M, p.K, p.N, a["rowptr"], a["colind"], a["vals"], a["B"], C)
+        if i == 1:
+            torch.cuda.synchronize()
+            spmm.spmm_pool_release()
+        outs.append(C)
+    torch.cuda.synchronize()
+    H.assert_within(outs[0], C_ref, S, "f32", "one-call")
+    for C in outs[1:]:
+        assert torch.equal(C, outs[0])
+    bad = a["rowptr"].clone()
+    bad[-1] = -5
+    C = torch.empty((p.M, p.N), device="cuda")
+    with pytest.raises(spmm.SpmmError) as err:
+        spmm.spmm_csr_f32(p.M, p.K, p.N, bad, a["colind"], a["vals"], a["B"], C)
+    assert err.value.status == 2  # SPMM_ERR_INVALID_CSR
+
+
 def test_side_stream():
     p = mixed(12, N=32)
     s = torch.cuda.Stream()
@@ -207,3 +233,4 @@ def test_column_tile_cap(kernel, b_dtype, cap):
     H.assert_within(C, C_ref, S, b_dtype, f"{kernel}/{b_dtype}/cap={cap}")
     with pytest.raises(spmm.SpmmError):
         spmm.spmm_plan_set_column_tile(plan, -1)
+
