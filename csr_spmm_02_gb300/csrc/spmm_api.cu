@@ -90,6 +90,8 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
     if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
   } else if (window_tc) {
     e = launch_tc_window_bf16(L);
+    // no tensor-map encoder in this driver: the row kernel instead
+    if (e == cudaErrorNotSupported) e = launch_row_bf16(L, s);
     if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
   } else if (window) {
     e = bf16 ? launch_window_bf16(L) : launch_window_f32(L);

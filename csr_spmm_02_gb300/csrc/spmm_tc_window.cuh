@@ -5,31 +5,51 @@
 // For rows whose columns are local (a band), the window kernel's work is a
 // dense product per row block: A_w (rows x window columns, zero where A has no
 // entry) times B_w (window columns x N).  On CUDA cores that product is bound
-// by the FP32 pipe; here a CTA of 128 rows hands it to tcgen05.mma:
+// by the FP32 pipe; here each 128-row tile hands it to tcgen05.mma:
 //
 //  * A's fp32 values are split exactly into three bf16 terms (hi + mid + lo
 //    carries all 24 significand bits); each bf16 x bf16 product is exact in
 //    fp32, so three MMAs per K-step reproduce the fp32 products and only the
 //    accumulation order differs from a row loop;
-//  * the window is walked in chunks of 64 columns: per chunk the CTA zeroes the
-//    three A tiles, scatters its rows' values into them (K-major core
-//    matrices), copies the chunk's 64 B rows straight into MN-major core
-//    matrices with 16-byte cp.async (rows past K are zero-filled), and one
-//    thread issues 4 K-steps x 3 terms of M=128, N, K=16 MMAs into the tensor
-//    memory accumulator, committing to an mbarrier that the CTA waits on
-//    (bounded) before it reuses the tiles;
-//  * the epilogue reads the accumulator with tcgen05.ld (warp w reads lanes
-//    32*(w%4).. and half (w/4) of the columns) and stores the rows.
+//  * the tile's window (at most three chunks of 64 columns) is built once in
+//    shared memory as three K-major bf16 tiles per chunk; B is streamed in
+//    32-row pieces by the tensor memory accelerator (one 32 x 8 box per 16
+//    bytes of row, landing directly in the MN-major core-matrix layout, rows
+//    past K zero-filled) through three stages;
+//  * per chunk, 4 K-steps x 3 terms of M=128, N, K=16 MMAs accumulate into one
+//    of two tensor-memory accumulators.
 //
-// A tile whose column span exceeds four chunks, or one with a row whose
-// columns do not strictly increase (duplicates), is computed by per-row
-// gathers in the same launch.  The dense product multiplies absent entries
+// The kernel is persistent (one CTA per SM, tiles strided by the grid) and
+// its warps have four roles, so that the steps of consecutive tiles overlap:
+//
+//  * warps 0-7 (builders) hold a tile's nonzeros in registers, check them
+//    (span, and strictly increasing columns in each row, from a bitmask of
+//    row starts), publish the tile's description, then zero and fill the A
+//    window once the previous tile's MMAs have read it;
+//  * warp 8 (producer) loads the B chunks of each tensor-core tile with TMA;
+//  * warp 9 (MMA) issues the MMAs once the A window and a B stage are full;
+//    tcgen05.commit frees the stage and the window and, per tile, marks the
+//    accumulator full;
+//  * warps 10-13 (epilogue) read a full accumulator with tcgen05.ld (warp w
+//    reads lanes 32*(w%4)..), turn each 32 x 32 block around in shared memory
+//    so that every store writes 4 rows x 128 contiguous bytes, then mark the
+//    accumulator drained.
+//
+// Every wait on an mbarrier is bounded: on expiry the kernel records
+// kErrStageTimeout in the plan's error word and stops instead of hanging.
+//
+// A tile whose column span exceeds three chunks, one holding more than 8192
+// nonzeros, or one with a row whose columns do not strictly increase
+// (duplicates) is computed by the builders with per-row gathers; a tile with
+// no nonzeros stores zero rows.  The dense product multiplies absent entries
 // as zeros, so a NaN/Inf in a B row inside the window reaches every row of
 // the tile; IEEE special values are outside the accepted inputs.
 #pragma once
 
+#include <algorithm>
 #include <climits>
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "spmm_device.cuh"
@@ -39,21 +59,40 @@ namespace spmm {
 
 namespace tc {
 
-constexpr int kRows = 128;       // rows per CTA = MMA M
+constexpr int kRows = 128;       // rows per tile = MMA M
 constexpr int kChunk = 64;       // window columns per chunk (4 K-steps of 16)
-constexpr int kMaxChunks = 4;    // larger spans use the gather path
+constexpr int kMaxChunks = 3;    // larger spans use the gather path
 constexpr int kKStride = 128;    // bytes between K-adjacent core matrices (8 rows x 16 bytes)
-constexpr int kMNStride = 1024;  // bytes between M/N-adjacent core matrices (8 along K per chunk)
-constexpr int kATile = kRows * kChunk * 2;  // one bf16 term: 16 KB
-constexpr int kPerThread = 32;   // nonzeros a thread holds: a tile of at most 8192 uses the tensor cores
-// the column exchange (4 bytes per held nonzero) and the row ids (1 byte) use the A tiles' space
-static_assert(kPerThread * 256 * 5 <= 3 * kATile, "exchange area");
+constexpr int kMNStride = 1024;  // A: bytes between M-adjacent core matrices (8 along K per chunk)
+constexpr int kBRows = 32;       // B rows per stage (2 K-steps)
+constexpr int kBMNStride = kBRows * 16;  // B: bytes between N-adjacent core matrices
+constexpr int kStages = 3;
+constexpr int kATile = kRows * kChunk * 2;         // one bf16 term of one chunk: 16 KB
+constexpr int kAWindow = kMaxChunks * 3 * kATile;  // the whole window: 144 KB
+constexpr int kBuilders = 256;                     // builder threads (warps 0-7)
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kEpiWarp0 = 10;  // warps 10-13
+constexpr int kCtaThreads = 14 * 32;
+constexpr int kPerThread = 32;  // nonzeros a builder holds: a tile of at most 8192 uses the tensor cores
+constexpr int kTileNnz = kPerThread * kBuilders;
+enum TileKind { kTensor = 0, kZero = 1, kGather = 2 };
+constexpr int kTwFloats = 32 * 36;  // one epilogue warp's transpose buffer (rows of 36 floats)
+// mbarriers: A full, A free, B full[3], B empty[3], accumulator full[2] and
+// drained[2], tile description full[2] and consumed[2]
+constexpr int kBars = 16;
+
+__host__ __device__ constexpr size_t stage_bytes(int N) { return size_t(kBRows) * N * 2; }
 
 __host__ __device__ constexpr size_t smem_bytes(int N) {
-  return size_t(3) * kATile          // A terms hi, mid, lo
-         + size_t(kChunk) * N * 2    // B chunk
-         + (kRows + 8) * 4           // rowptr slice
-         + 64;                       // mbarrier, TMEM address, reductions
+  return size_t(kAWindow) + kStages * stage_bytes(N)  // A window, B stages
+         + kTileNnz                                   // local row of every held nonzero (1 byte)
+         + (kBuilders / 32) * kPerThread * 4          // each builder warp's last-lane columns
+         + kTileNnz / 8                               // row-start bitmask over the held nonzeros
+         + 4 * kTwFloats * 4                          // epilogue transposes
+         + (kRows + 8) * 4                            // rowptr slice
+         + kBars * 8 + 2 * 16 + 2 * 8 + 4 + 4 * 4 + 4;  // barriers, tile descriptions, ring, TMEM
+                                                         // address, reductions, beat
 }
 
 // Shared-memory matrix descriptor: no swizzle, canonical core-matrix layout
@@ -90,284 +129,521 @@ __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::be
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// 8 consecutive fp32 accumulator columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
+// 16 consecutive fp32 accumulator columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ uint16_t bf16_rn_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
+// Plain arrive (release semantics at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// One 2-D TMA box of B (8 columns x 32 rows, 512 bytes) into shared memory,
+// completing its bytes on `bar`.  x (the column) is a multiple of 8.
+__device__ __forceinline__ void tma_load_b(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Barrier 1 joins the builder warps only.
+__device__ __forceinline__ void builders_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kBuilders) : "memory"); }
+// The same barrier, returning whether `p` holds in every builder thread.
+__device__ __forceinline__ bool builders_and(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, %2, a;\n\tselp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(p)), "n"(kBuilders)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that tolerates slow builders: the poll budget restarts while
+// `beat` (advanced by the builders per tile and per gathered row) moves, so it
+// expires only when the builders make no progress.
+__device__ __forceinline__ bool mbar_wait_progress(uint32_t bar, uint32_t parity, const volatile int* beat) {
+  int seen = *beat;
+  for (;;) {
+    if (mbar_wait_bounded(bar, parity, kSpinLimit)) return true;
+    const int now = *beat;
+    if (now == seen) return false;
+    seen = now;
+  }
+}
+
+// Hint: bring [lo, hi) into L2, shrunk to 16-byte boundaries inside the range.
+__device__ __forceinline__ void l2_prefetch(const void* lo, const void* hi) {
+  const uintptr_t a = (reinterpret_cast<uintptr_t>(lo) + 15) & ~uintptr_t(15);
+  const uintptr_t e = reinterpret_cast<uintptr_t>(hi) & ~uintptr_t(15);
+  if (e > a)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(uint32_t(e - a)) : "memory");
+}
+
 }  // namespace tc
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(tc::kCtaThreads, 1)
     spmm_tc_window_kernel(int32_t M, int32_t N, int32_t K, const int32_t* __restrict__ rowptr,
                           const int32_t* __restrict__ colind, const float* __restrict__ vals,
                           const uint16_t* __restrict__ B, float* __restrict__ C, int* __restrict__ err,
-                          uint32_t tmem_cols) {
+                          uint32_t acc_cols, const __grid_constant__ CUtensorMap bmap) {
   using namespace tc;
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* s_A = smem;                                // 3 x [16 row groups][8 k groups][8][8] bf16
-  unsigned char* s_B = smem + 3 * kATile;                   // [N/8 n groups][8 k groups][8][8] bf16
-  int* s_rp = reinterpret_cast<int*>(s_B + size_t(kChunk) * N * 2);
+  const size_t sb = stage_bytes(N);
+  unsigned char* s_A = smem;                                  // chunk c, term t at (3c + t) * kATile
+  unsigned char* s_B = smem + kAWindow;                       // stage s at s * sb
+  uint8_t* s_rowid = s_B + kStages * sb;                      // [kTileNnz] local row of each held nonzero
+  int* s_last = reinterpret_cast<int*>(s_rowid + kTileNnz);  // [8 warps][kPerThread] lane 31's columns
+  uint32_t* s_start = reinterpret_cast<uint32_t*>(s_last + (kBuilders / 32) * kPerThread);  // row-start bits
+  float* s_tw = reinterpret_cast<float*>(s_start + kTileNnz / 32);  // [4 warps][kTwFloats]
+  int* s_rp = reinterpret_cast<int*>(s_tw + 4 * kTwFloats);   // [kRows + 8] rowptr slice
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_rp + kRows + 8);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 1);
-  int* s_red = reinterpret_cast<int*>(s_tmem + 1);  // [0] min col, [1] max col, [2] flags
+  int4* s_info = reinterpret_cast<int4*>(s_bar + kBars);      // [2] (first row, rows, cmin, kind | chunks << 8)
+  int* s_ring = reinterpret_cast<int*>(s_info + 2);           // [2][2] first row and rows per accumulator
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ring + 4);
+  int* s_red = reinterpret_cast<int*>(s_tmem + 1);            // [0] min col, [1] max col, [2] flags
+  volatile int* s_beat = s_red + 4;                           // builders' progress counter
 
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const int i0 = blockIdx.x * kRows;
-  const int nrows = min(kRows, M - i0);
-  const uint64_t stream_pol = policy_evict_first();
+  const int ntiles = int((int64_t(M) + kRows - 1) / kRows);
+  const uint32_t bar0 = smem_addr(s_bar);
+  auto bar = [bar0](int i) { return bar0 + 8u * uint32_t(i); };
+  constexpr int kAFull = 0, kAFree = 1, kBFull = 2, kBEmpty = 5, kAccFull = 8, kAccDrained = 10, kInfoFull = 12,
+                kInfoUsed = 14;
 
-  // ---- set-up: tensor memory, barrier, rowptr slice ----------------------
+  // ---- set-up: two accumulators of acc_cols columns, the barriers ----------
   if (w == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(s_tmem)),
-                 "r"(tmem_cols)
+                 "r"(2 * acc_cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    mbar_init(smem_addr(s_bar), 1);
-    s_red[0] = INT_MAX;
-    s_red[1] = -1;
-    s_red[2] = 0;
+    *s_beat = 0;
+    mbar_init(bar(kAFull), 1);   // the builders, once the window is written
+    mbar_init(bar(kAFree), 1);   // commit after a tile's last MMAs
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBFull + s), 1);   // the producer's expect-tx arrive + the TMA bytes
+      mbar_init(bar(kBEmpty + s), 1);  // commit after the stage's MMAs
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kAccFull + s), 2);        // the tile's last commit + the ring entry's arrive
+      mbar_init(bar(kAccDrained + s), 4);     // one arrive per epilogue warp
+      mbar_init(bar(kInfoFull + s), 1);       // the builders publish a tile description
+      mbar_init(bar(kInfoUsed + s), 2);       // the producer and the MMA warp have read it
+    }
   }
-  for (int t = tid; t <= nrows; t += kThreads) s_rp[t] = ld_stream(rowptr + i0 + t, stream_pol);
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t bar = smem_addr(s_bar);
 
-  // ---- the tile's nonzeros into registers (one load round) ---------------
-  // Thread t holds nonzeros p0 + t + 256 i (i < kPerThread): its value and a
-  // packed word, (row << 16) | (column & 0xFFFF), or kNone past the tile.
-  constexpr uint32_t kNone = 0xFFFFFFFFu;
-  const int p0 = s_rp[0], p1 = s_rp[nrows];
-  const bool fits = p1 - p0 <= kThreads * kPerThread;
-  uint32_t pk[kPerThread];
-  float val[kPerThread];
-  if (fits) {
-    // all loads first (one latency), then the columns go through shared
-    // memory (the A tiles are still free) so each thread can see the column
-    // of the nonzero before each of its own
-    int* s_cols = reinterpret_cast<int*>(s_A);  // [kPerThread][kThreads]
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-      const int g = p0 + tid + kThreads * i;
-      pk[i] = g < p1 ? uint32_t(ld_stream(colind + g, stream_pol)) : kNone;
-      val[i] = g < p1 ? ld_stream(vals + g, stream_pol) : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) s_cols[i * kThreads + tid] = int(pk[i]);
-    // the local row of every tile nonzero, one byte each (warp w fills rows w, w+8, ...)
-    uint8_t* s_rowid = reinterpret_cast<uint8_t*>(s_cols + kPerThread * kThreads);
-    for (int r = w; r < nrows; r += kThreads / 32)
-      for (int g = s_rp[r] + lane; g < s_rp[r + 1]; g += 32) s_rowid[g - p0] = uint8_t(r);
-  }
-  __syncthreads();
-  if (fits) {
-    const int* s_cols = reinterpret_cast<const int*>(s_A);
-    const uint8_t* s_rowid = reinterpret_cast<const uint8_t*>(s_cols + kPerThread * kThreads);
-    int lo = INT_MAX, hi = -1;
-    bool inc = true;
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-      const int g = p0 + tid + kThreads * i;
-      if (g < p1) {
-        const int c = int(pk[i]);
-        lo = min(lo, c);
-        hi = max(hi, c);
-        const int r = s_rowid[g - p0];
-        if (g > s_rp[r])  // the previous nonzero is in the same row
-          inc &= c > s_cols[tid > 0 ? i * kThreads + tid - 1 : (i - 1) * kThreads + kThreads - 1];
-        pk[i] = (uint32_t(r) << 16) | (uint32_t(c) & 0xFFFFu);
-      }
-    }
-    lo = __reduce_min_sync(0xffffffffu, lo);
-    hi = __reduce_max_sync(0xffffffffu, hi);
-    const bool all_inc = __all_sync(0xffffffffu, inc);
-    if (lane == 0) {
-      atomicMin(s_red + 0, lo);
-      atomicMax(s_red + 1, hi);
-      if (!all_inc) atomicOr(s_red + 2, 1);
-    }
-  } else if (tid == 0) {
-    s_red[2] = 1;  // too many nonzeros to hold: gather path
-  }
-  __syncthreads();
-  const int cmin = s_red[0], cmax = s_red[1];
-  const int nchunks = cmax < 0 ? 0 : (cmax - cmin) / kChunk + 1;
-  const bool use_tc = s_red[2] == 0 && nchunks <= kMaxChunks;
-
-  if (use_tc && nchunks > 0) {
-    // local column of each held nonzero: its low 16 bits minus cmin's, modulo
-    // 2^16 (exact, since the span is below 2^16)
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i)
-      if (pk[i] != kNone) pk[i] = (pk[i] & 0xFFFF0000u) | ((pk[i] - uint32_t(cmin)) & 0xFFFFu);
-    const uint32_t id = idesc(N);
-    const uint32_t a_base = smem_addr(s_A), b_base = smem_addr(s_B);
-    // B rows c0 .. c0+63 of chunk ch (16-byte chunks: row k, column group q)
-    const int qn = N / 8;
-    auto issue_b = [&](int ch) {
-      const int c0 = cmin + ch * kChunk;
-      const uint32_t base = b_base;
-      for (int t = tid; t < kChunk * qn; t += kThreads) {
-        const int k = t / qn, q = t - k * qn;
-        const int j = c0 + k;
-        const uint32_t dst = base + uint32_t(q) * kMNStride + uint32_t(k >> 3) * kKStride + uint32_t(k & 7) * 16;
-        cp_async16_zfill(dst, j < K ? static_cast<const void*>(B + size_t(j) * N + q * 8) : B, j < K);
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    };
+  if (w < kBuilders / 32) {
+    // =================== builders ===================
+    constexpr uint32_t kNone = 0xFFFFFFFFu;
+    const uint64_t stream_pol = policy_evict_first();
+    uint32_t tt = 0;  // tensor-core tiles built
     bool ok = true;
-    for (int ch = 0; ch < nchunks; ++ch) {
-      if (ch > 0) {  // the previous chunk's MMAs have read the tiles (decided by the whole CTA)
-        if (!__syncthreads_and(mbar_wait_bounded(bar, uint32_t(ch - 1) & 1u, kSpinLimit))) {
+    int j = 0;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++j) {
+      const int i0 = tile * kRows;
+      const int nrows = min(kRows, M - i0);
+      builders_sync();  // the previous tile is done with s_rp, s_red, s_rowid and s_last
+      for (int t = tid; t <= nrows; t += kBuilders) s_rp[t] = ld_stream(rowptr + i0 + t, stream_pol);
+      s_start[tid] = 0u;  // kTileNnz / 32 == kBuilders words
+      if (tid == 0) {
+        s_red[0] = INT_MAX;
+        s_red[1] = -1;
+        s_red[2] = 0;
+        *s_beat = *s_beat + 1;
+      }
+      // the next tile's nonzero range, for an L2 prefetch once this tile's loads are out
+      const int next = tile + int(gridDim.x);
+      int q0 = 0, q1 = 0;
+      if (tid == 32 && next < ntiles) {
+        q0 = __ldg(rowptr + int64_t(next) * kRows);
+        q1 = __ldg(rowptr + min(int64_t(M), int64_t(next) * kRows + kRows));
+      }
+      builders_sync();
+
+      // ---- the tile's nonzeros into registers (one load round) ----------
+      // Thread t holds nonzeros p0 + t + 256 i (i < kPerThread): its value and
+      // its column (later a packed word (row << 16) | local column), or kNone.
+      const int p0 = s_rp[0], p1 = s_rp[nrows];
+      const bool fits = p1 - p0 <= kTileNnz;
+      uint32_t pk[kPerThread];
+      float val[kPerThread];
+      if (fits) {
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i) {
+          const int g = p0 + tid + kBuilders * i;
+          pk[i] = g < p1 ? uint32_t(ld_stream(colind + g, stream_pol)) : kNone;
+          val[i] = g < p1 ? ld_stream(vals + g, stream_pol) : 0.f;
+        }
+      }
+      if (tid == 32 && q1 > q0 && q1 - q0 <= kTileNnz) {
+        l2_prefetch(colind + q0, colind + q1);
+        l2_prefetch(vals + q0, vals + q1);
+      }
+      if (fits) {
+        // the local row of every tile nonzero, one byte each (warp w fills rows w, w+8, ...)
+        for (int r = w; r < nrows; r += kBuilders / 32)
+          for (int g = s_rp[r] + lane; g < s_rp[r + 1]; g += 32) s_rowid[g - p0] = uint8_t(r);
+        // a bit per row start (an empty row starts nowhere)
+        for (int r = tid; r < nrows; r += kBuilders)
+          if (s_rp[r] < s_rp[r + 1]) {
+            const int pos = s_rp[r] - p0;
+            atomicOr(s_start + (pos >> 5), 1u << (pos & 31));
+          }
+        // lane 31's columns: the predecessors of the next warp's lane 0
+        if (lane == 31)
+#pragma unroll
+          for (int i = 0; i < kPerThread; ++i) s_last[w * kPerThread + i] = int(pk[i]);
+      }
+      builders_sync();
+      if (fits) {
+        // span, and strictly increasing columns inside each row: a nonzero
+        // that does not start a row must exceed its predecessor g-1, which is
+        // lane-1's, the previous warp's lane 31's, or for thread 0 thread
+        // 255's of the previous round.  Nonzero p0 + tid + 256 i is bit
+        // `lane` of row-start word w + 8 i.
+        int lo = INT_MAX, hi = -1;
+        bool inc = true;
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i) {
+          const int g = p0 + tid + kBuilders * i;
+          const int c = int(pk[i]);
+          const int up = __shfl_up_sync(0xffffffffu, c, 1);
+          const uint32_t word = s_start[w + (kBuilders / 32) * i];
+          const int prev = lane > 0 ? up
+                                    : (w > 0 ? s_last[(w - 1) * kPerThread + i]
+                                             : s_last[(kBuilders / 32 - 1) * kPerThread + (i > 0 ? i - 1 : 0)]);
+          const bool valid = g < p1;
+          const bool starts = (word >> lane) & 1u;
+          if (valid) {
+            lo = min(lo, c);
+            hi = max(hi, c);
+          }
+          inc &= !valid || starts || c > prev;
+          const int r = valid ? int(s_rowid[g - p0]) : 0;
+          pk[i] = valid ? (uint32_t(r) << 16) | (uint32_t(c) & 0xFFFFu) : kNone;
+        }
+        lo = __reduce_min_sync(0xffffffffu, lo);
+        hi = __reduce_max_sync(0xffffffffu, hi);
+        const bool all_inc = __all_sync(0xffffffffu, inc);
+        if (lane == 0) {
+          atomicMin(s_red + 0, lo);
+          atomicMax(s_red + 1, hi);
+          if (!all_inc) atomicOr(s_red + 2, 1);
+        }
+      } else if (tid == 0) {
+        s_red[2] = 1;  // too many nonzeros to hold: gather path
+      }
+      builders_sync();
+      const int cmin = s_red[0], cmax = s_red[1];
+      const int nch = cmax < 0 ? 0 : (cmax - cmin) / kChunk + 1;
+      const int kind = (s_red[2] != 0 || nch > kMaxChunks) ? kGather : (nch == 0 ? kZero : kTensor);
+
+      // ---- publish the tile's description to the producer and MMA warps ---
+      const uint32_t slot = uint32_t(j) & 1u;
+      bool got = true;
+      if (tid == 0) {
+        if (j >= 2) got = mbar_wait_bounded(bar(kInfoUsed + slot), (uint32_t(j >> 1) - 1) & 1u, kSpinLimit);
+        s_info[slot] = make_int4(i0, nrows, cmin, kind | (nch << 8));
+        mbar_arrive(bar(kInfoFull + slot));
+      }
+      if (!builders_and(got)) {
+        ok = false;
+        break;
+      }
+
+      if (kind == kTensor) {
+        // local column of each held nonzero: its low 16 bits minus cmin's,
+        // modulo 2^16 (exact, since the span is below 2^16)
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i)
+          if (pk[i] != kNone) pk[i] = (pk[i] & 0xFFFF0000u) | ((pk[i] - uint32_t(cmin)) & 0xFFFFu);
+        if (tt >= 1) {  // the previous tile's MMAs have read the window
+          ok = builders_and(mbar_wait_bounded(bar(kAFree), (tt - 1) & 1u, kSpinLimit));
+          fence_after();
+          if (!ok) break;
+        }
+        for (int t = tid; t < nch * 3 * kATile / 16; t += kBuilders)
+          reinterpret_cast<uint4*>(s_A)[t] = make_uint4(0u, 0u, 0u, 0u);
+        builders_sync();
+        // every held nonzero into its chunk: value -> three bf16 terms
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i) {
+          if (pk[i] != kNone) {
+            const int k = int(pk[i] & 0xFFFFu), r = int(pk[i] >> 16);
+            const int ch = k >> 6, kk = k & (kChunk - 1);
+            const float v = val[i];
+            const uint16_t h = bf16_rn_bits(v);
+            const float r1 = v - bf16_bits_to_float(h);
+            const uint16_t m = bf16_rn_bits(r1);
+            const uint16_t l = bf16_rn_bits(r1 - bf16_bits_to_float(m));
+            const uint32_t off = uint32_t(3 * ch) * kATile + uint32_t(r >> 3) * kMNStride +
+                                 uint32_t(kk >> 3) * kKStride + uint32_t(r & 7) * 16 + uint32_t(kk & 7) * 2;
+            *reinterpret_cast<uint16_t*>(s_A + off) = h;
+            *reinterpret_cast<uint16_t*>(s_A + kATile + off) = m;
+            *reinterpret_cast<uint16_t*>(s_A + 2 * kATile + off) = l;
+          }
+        }
+        fence_proxy_async();  // generic-proxy writes become visible to the tensor cores
+        builders_sync();
+        if (tid == 0) mbar_arrive(bar(kAFull));
+        ++tt;
+      } else if (kind == kZero) {  // no nonzeros in the tile: zero rows
+        for (int t = tid; t < nrows * (N / 4); t += kBuilders) {
+          const int r = t / (N / 4), c4 = t - r * (N / 4);
+          st_stream4(C + size_t(i0 + r) * N + 4 * c4, 0.f, 0.f, 0.f, 0.f);
+        }
+      } else {  // gather path: warp w computes rows w, w + 8, ... (8 columns per lane per pass)
+        for (int r = w; r < nrows; r += kBuilders / 32) {
+          const int start = s_rp[r], end = s_rp[r + 1];
+          if (tid == 0) *s_beat = *s_beat + 1;
+          for (int c0 = lane * 8; c0 < N; c0 += 32 * 8) {
+            FVec<8> acc;
+            acc.zero();
+            for (int g = start; g < end; ++g) {
+              const int c = __ldg(colind + g);
+              BSlice<uint16_t, 8> bs;
+              bs.load(B + size_t(c) * N + c0);
+              FVec<8> bv;
+              bs.widen(bv);
+              acc.fma(pair(__ldg(vals + g)), bv);
+            }
+            store_c<8>(C + size_t(i0 + r) * N + c0, acc);
+          }
+        }
+      }
+    }
+    if (!ok && tid == 0) atomicOr(err, kErrStageTimeout);
+  } else if (w == kProducerWarp) {
+    // =================== producer: B chunks by TMA ===================
+    if (lane == 0) {
+      uint32_t gc = 0;  // B pieces loaded (stage gc % kStages)
+      bool ok = true;
+      int j = 0;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++j) {
+        const uint32_t slot = uint32_t(j) & 1u;
+        if (!mbar_wait_progress(bar(kInfoFull + slot), uint32_t(j >> 1) & 1u, s_beat)) {
+          ok = false;
+          break;
+        }
+        const int4 info = s_info[slot];
+        mbar_arrive(bar(kInfoUsed + slot));
+        if ((info.w & 0xFF) != kTensor) continue;
+        const int pieces = (info.w >> 8) * (kChunk / kBRows);
+        for (int c = 0; c < pieces; ++c) {
+          const uint32_t s = gc % kStages, use = gc / kStages;
+          if (use >= 1 && !mbar_wait_bounded(bar(kBEmpty + s), (use - 1) & 1u, kSpinLimit)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBFull + s), uint32_t(sb));
+          const uint32_t dst = smem_addr(s_B + s * sb);
+          for (int q = 0; q < N / 8; ++q)
+            tma_load_b(dst + uint32_t(q) * kBMNStride, &bmap, 8 * q, info.z + c * kBRows, bar(kBFull + s));
+          ++gc;
+        }
+      }
+      if (!ok) atomicOr(err, kErrStageTimeout);
+    }
+  } else if (w == kMmaWarp) {
+    // =================== MMA issue ===================
+    if (lane == 0) {
+      const uint32_t id = idesc(N);
+      const uint32_t a_base = smem_addr(s_A), b_base = smem_addr(s_B);
+      uint32_t gc = 0, tt = 0;  // B pieces and tensor-core tiles issued
+      bool ok = true;
+      int j = 0;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++j) {
+        const uint32_t slot = uint32_t(j) & 1u;
+        if (!mbar_wait_progress(bar(kInfoFull + slot), uint32_t(j >> 1) & 1u, s_beat)) {
+          ok = false;
+          break;
+        }
+        const int4 info = s_info[slot];
+        mbar_arrive(bar(kInfoUsed + slot));
+        if ((info.w & 0xFF) != kTensor) continue;
+        const int nch = info.w >> 8;
+        const uint32_t b = tt & 1u, ub = tt >> 1;
+        // the window is built, and the epilogue has read this accumulator's previous tile
+        if (!mbar_wait_progress(bar(kAFull), tt & 1u, s_beat) ||
+            (ub >= 1 && !mbar_wait_bounded(bar(kAccDrained + b), (ub - 1) & 1u, kSpinLimit))) {
           ok = false;
           break;
         }
         fence_after();
-      }
-      issue_b(ch);  // in flight while the A tiles are built
-      // zero the three A tiles
-      for (int t = tid; t < 3 * kATile / 16; t += kThreads)
-        reinterpret_cast<uint4*>(s_A)[t] = make_uint4(0u, 0u, 0u, 0u);
-      __syncthreads();
-      // scatter the held nonzeros of this chunk: value -> three bf16 terms
-#pragma unroll
-      for (int i = 0; i < kPerThread; ++i) {
-        const int k = int(pk[i] & 0xFFFFu) - ch * kChunk;
-        if (pk[i] != kNone && k >= 0 && k < kChunk) {
-          const int r = int(pk[i] >> 16);
-          const float v = val[i];
-          const uint16_t h = bf16_rn_bits(v);
-          const float r1 = v - bf16_bits_to_float(h);
-          const uint16_t m = bf16_rn_bits(r1);
-          const uint16_t l = bf16_rn_bits(r1 - bf16_bits_to_float(m));
-          const uint32_t off = uint32_t(r >> 3) * kMNStride + uint32_t(k >> 3) * kKStride + uint32_t(r & 7) * 16 +
-                               uint32_t(k & 7) * 2;
-          *reinterpret_cast<uint16_t*>(s_A + off) = h;
-          *reinterpret_cast<uint16_t*>(s_A + kATile + off) = m;
-          *reinterpret_cast<uint16_t*>(s_A + 2 * kATile + off) = l;
-        }
-      }
-      asm volatile("cp.async.wait_group 0;" ::: "memory");  // this chunk's B rows
-      fence_proxy_async();  // generic-proxy writes become visible to the tensor cores
-      fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        fence_after();
-        const uint32_t bbuf = b_base;
-#pragma unroll
-        for (int ks = 0; ks < kChunk / 16; ++ks) {
-#pragma unroll
-          for (int term = 0; term < 3; ++term) {
-            const uint64_t a = sdesc(a_base + uint32_t(term) * kATile + uint32_t(2 * ks) * kKStride, kKStride, kMNStride);
-            const uint64_t b = sdesc(bbuf + uint32_t(2 * ks) * kKStride, kKStride, kMNStride);
-            mma(tmem, a, b, id, ch > 0 || ks > 0 || term > 0);
+        const uint32_t acc = tmem + b * acc_cols;
+        // piece c holds B rows cmin + 32c ..: K-steps 2c, 2c+1 of the window
+        for (int c = 0; c < nch * (kChunk / kBRows) && ok; ++c) {
+          const uint32_t s = gc % kStages, use = gc / kStages;
+          if (!mbar_wait_bounded(bar(kBFull + s), use & 1u, kSpinLimit)) {
+            ok = false;
+            break;
           }
+          fence_after();
+          const int ch = c / (kChunk / kBRows), kp = c % (kChunk / kBRows);
+#pragma unroll
+          for (int ks = 0; ks < kBRows / 16; ++ks) {
+#pragma unroll
+            for (int term = 0; term < 3; ++term) {
+              const uint64_t a = sdesc(a_base + uint32_t(3 * ch + term) * kATile +
+                                           uint32_t(2 * (kp * (kBRows / 16) + ks)) * kKStride,
+                                       kKStride, kMNStride);
+              const uint64_t bd = sdesc(b_base + s * uint32_t(sb) + uint32_t(2 * ks) * kKStride, kKStride, kBMNStride);
+              mma(acc, a, bd, id, c > 0 || ks > 0 || term > 0);
+            }
+          }
+          commit(bar(kBEmpty + s));  // the stage is free once these MMAs have read it
+          ++gc;
         }
-        commit(bar);
+        if (!ok) break;
+        commit(bar(kAFree));  // the window too
+        s_ring[2 * b] = info.x;
+        s_ring[2 * b + 1] = info.y;
+        commit(bar(kAccFull + b));  // the accumulator is complete once the MMAs are
+        mbar_arrive(bar(kAccFull + b));
+        ++tt;
       }
+      // end marker in the next accumulator's ring entry
+      const uint32_t b = tt & 1u, ub = tt >> 1;
+      if (ub >= 1 && !mbar_wait_bounded(bar(kAccDrained + b), (ub - 1) & 1u, kSpinLimit)) ok = false;
+      s_ring[2 * b] = -1;
+      s_ring[2 * b + 1] = 0;
+      mbar_arrive(bar(kAccFull + b));
+      mbar_arrive(bar(kAccFull + b));
+      // the last tile's commits have arrived before the CTA's shared memory goes away
+      if (tt >= 1 && !mbar_wait_bounded(bar(kAFree), (tt - 1) & 1u, kSpinLimit)) ok = false;
+      if (!ok) atomicOr(err, kErrStageTimeout);
     }
-    if (ok) ok = __syncthreads_and(mbar_wait_bounded(bar, uint32_t(nchunks - 1) & 1u, kSpinLimit));
-    if (!ok) {  // the tensor cores did not finish: report, write nothing
-      if (tid == 0) atomicOr(err, kErrStageTimeout);
-    } else {
+  } else {
+    // =================== epilogue ===================
+    // Warp w reads accumulator lanes 32*(w%4).. (rows 32*(w%4).. of the
+    // tile) 32 columns at a time; a per-warp shared-memory transpose (rows of
+    // 36 floats) turns them into 4-row x 128-byte coalesced stores.
+    const int q = w & 3;
+    float* tw = s_tw + (w - kEpiWarp0) * kTwFloats;
+    const int rr = lane >> 3, cc = (lane & 7) * 4;  // store phase: row (of 4) and column of this lane
+    for (uint32_t k = 0;; ++k) {
+      const uint32_t b = k & 1u, use = k >> 1;
+      if (!mbar_wait_progress(bar(kAccFull + b), use & 1u, s_beat)) {
+        if (lane == 0) atomicOr(err, kErrStageTimeout);
+        break;
+      }
       fence_after();
-      // epilogue: warp w reads lanes 32*(w%4).. (its 32 rows) and half w/4 of
-      // the columns, 32 at a time; a per-warp shared-memory transpose (rows of
-      // 36 floats) turns them into 4-row x 128-byte coalesced stores
-      const int q = w & 3, half = w >> 2;
-      const int cols = N / 2;
-      float* tw = reinterpret_cast<float*>(s_A) + w * (32 * 36);
-      const int rr = lane >> 3, cc = (lane & 7) * 4;  // store phase: row (of 4) and column of this lane
-      for (int c = half * cols; c < (half + 1) * cols; c += 32) {  // N/2 is a multiple of 8
-        const int n8 = min(32, (half + 1) * cols - c) / 8;
-        uint32_t v[4][8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (j < n8) tc::tmem_ld8(tmem + (uint32_t(32 * q) << 16) + uint32_t(c + 8 * j), v[j]);
+      const int i0 = s_ring[2 * b], nrows = s_ring[2 * b + 1];
+      if (i0 < 0) break;
+      const uint32_t acc = tmem + b * acc_cols + (uint32_t(32 * q) << 16);
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t v0[16], v1[16];
+        const bool two = c0 + 16 < N;  // N is a multiple of 16
+        tmem_ld16(acc + uint32_t(c0), v0);
+        if (two) tmem_ld16(acc + uint32_t(c0 + 16), v1);
         tmem_wait_ld();
-        __syncwarp();
+        __syncwarp();  // every lane is done reading the previous block
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          *reinterpret_cast<uint4*>(tw + lane * 36 + 8 * j) = make_uint4(v[j][0], v[j][1], v[j][2], v[j][3]);
-          *reinterpret_cast<uint4*>(tw + lane * 36 + 8 * j + 4) = make_uint4(v[j][4], v[j][5], v[j][6], v[j][7]);
-        }
-        __syncwarp();
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<uint4*>(tw + lane * 36 + e) = make_uint4(v0[e], v0[e + 1], v0[e + 2], v0[e + 3]);
+        if (two)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // rows 4k .. 4k+3 of the warp's 32
-          const int lr = 4 * k + rr;
-          const int row = i0 + 32 * q + lr;
-          if (row < M && cc < 8 * n8) {
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<uint4*>(tw + lane * 36 + 16 + e) = make_uint4(v1[e], v1[e + 1], v1[e + 2], v1[e + 3]);
+        __syncwarp();
+        const int ncols = two ? 32 : 16;
+#pragma unroll
+        for (int k8 = 0; k8 < 8; ++k8) {  // rows 4k8 .. 4k8+3 of the warp's 32
+          const int lr = 4 * k8 + rr;
+          if (32 * q + lr < nrows && cc < ncols) {
             const float4 x = *reinterpret_cast<const float4*>(tw + lr * 36 + cc);
-            st_stream4(C + size_t(row) * N + c + cc, x.x, x.y, x.z, x.w);
+            st_stream4(C + (size_t(i0) + size_t(32 * q + lr)) * N + c0 + cc, x.x, x.y, x.z, x.w);
           }
         }
       }
-    }
-  } else if (use_tc) {  // no nonzeros in the tile: zero rows
-    for (int t = tid; t < nrows * (N / 4); t += kThreads) {
-      const int r = t / (N / 4), c4 = t - r * (N / 4);
-      st_stream4(C + size_t(i0 + r) * N + 4 * c4, 0.f, 0.f, 0.f, 0.f);
-    }
-  } else {  // gather path: warp w computes rows w, w + 8, ... (8 columns per lane per pass)
-    for (int r = w; r < nrows; r += kThreads / 32) {
-      const int start = s_rp[r], end = s_rp[r + 1];
-      for (int c0 = lane * 8; c0 < N; c0 += 32 * 8) {
-        FVec<8> acc;
-        acc.zero();
-        for (int g = start; g < end; ++g) {
-          const int c = __ldg(colind + g);
-          BSlice<uint16_t, 8> bs;
-          bs.load(B + size_t(c) * N + c0);
-          FVec<8> b;
-          bs.widen(b);
-          acc.fma(pair(__ldg(vals + g)), b);
-        }
-        store_c<8>(C + size_t(i0 + r) * N + c0, acc);
-      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kAccDrained + b));
     }
   }
 
-  // ---- release the tensor memory -----------------------------------------
+  // ---- release the tensor memory -------------------------------------------
   fence_before();
   __syncthreads();
   if (w == 0) {
     fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * acc_cols) : "memory");
   }
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// B (K x N bf16, row-major) as a 2-D tensor for TMA: boxes of 8 columns x 32 rows.
+inline cudaError_t make_b_map(const uint16_t* B, int32_t K, int32_t N, CUtensorMap* map) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(K)};
+  const cuuint64_t strides[1] = {cuuint64_t(N) * 2};
+  const cuuint32_t box[2] = {8, uint32_t(tc::kBRows)};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(B), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// N a multiple of 16 up to 256, B and C 16-byte aligned (checked by exec).
 inline cudaError_t launch_tc_window(const Launch& L) {
-  const size_t smem = tc::smem_bytes(L.N);
+  if (L.nnz == 0) return cudaMemsetAsync(L.C, 0, size_t(L.M) * size_t(L.N) * sizeof(float), L.stream);
   static bool attr_set[kMaxDevices] = {};
+  static int sm_count[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= kMaxDevices || !attr_set[dev]) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(spmm_tc_window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(tc::smem_bytes(256)));
     if (e != cudaSuccess) return e;
-    if (dev < kMaxDevices) attr_set[dev] = true;
+    if ((e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    attr_set[dev] = true;
   }
-  uint32_t cols = 32;
+  CUtensorMap map;
+  if ((e = make_b_map(static_cast<const uint16_t*>(L.B), L.K, L.N, &map)) != cudaSuccess) return e;
+  uint32_t cols = 32;  // one accumulator: a power of two >= N
   while (cols < uint32_t(L.N)) cols <<= 1;
-  const unsigned grid = unsigned((int64_t(L.M) + tc::kRows - 1) / tc::kRows);
-  spmm_tc_window_kernel<<<grid, kThreads, smem, L.stream>>>(L.M, L.N, L.K, L.rowptr, L.colind, L.vals,
-                                                            static_cast<const uint16_t*>(L.B), L.C, L.err, cols);
+  const int64_t tiles = (int64_t(L.M) + tc::kRows - 1) / tc::kRows;
+  const unsigned grid = unsigned(std::min<int64_t>(tiles, sm_count[dev]));
+  spmm_tc_window_kernel<<<grid, tc::kCtaThreads, tc::smem_bytes(L.N), L.stream>>>(
+      L.M, L.N, L.K, L.rowptr, L.colind, L.vals, static_cast<const uint16_t*>(L.B), L.C, L.err, cols, map);
   return cudaGetLastError();
 }
 

@@ -98,11 +98,11 @@ typedef enum {
                               * For N > 8 exec runs the row kernel instead. */
   SPMM_KERNEL_WINDOW_TC = 5  /* the window kernel's dense product on the tensor cores
                               * (tcgen05, accumulator in tensor memory) for bf16 B with
-                              * N a multiple of 16 up to 256: 128 rows per CTA, A's fp32
-                              * values split exactly into three bf16 terms, the window
-                              * walked in 64-column chunks; tiles with a span over 256
-                              * columns or duplicate columns gather per row.  Other B
-                              * types or widths run the window kernel. */
+                              * N a multiple of 16 up to 256: a persistent kernel over
+                              * 128-row tiles, A's fp32 values split exactly into three
+                              * bf16 terms, B streamed by TMA in 64-row chunks; tiles
+                              * with a span over 192 columns or duplicate columns gather
+                              * per row.  Other B types or widths run the window kernel. */
 } spmm_kernel;
 
 /* Opaque plan: owns its device workspace (merge-path partition, carry rows

@@ -129,9 +129,10 @@ def test_tc_banded_parity(N):
     assert info["kernel"] == "window_tc"
 
 
-@pytest.mark.parametrize("below,above", [(0, 0), (10, 20), (60, 3), (100, 90), (150, 150)])
+@pytest.mark.parametrize("below,above", [(0, 0), (10, 20), (60, 3), (32, 32), (33, 32), (100, 90), (150, 150)])
 def test_tc_spans_and_gather_fallback(below, above):
-    # 128-row tiles span 128 + below + above columns: 2 .. 4 chunks, then the gather path
+    # 128-row tiles span 128 + below + above columns: 2 or 3 chunks up to 192 columns (32, 32), then the
+    # gather path (33, 32 and wider)
     p = banded(below + above, 777, 900, below, above, 64, b_dtype="bf16")
     check(p, kernel="window_tc")
 
