@@ -23,9 +23,9 @@
 // its warps have four roles, so that the steps of consecutive tiles overlap:
 //
 //  * warps 0-7 (builders) hold a tile's nonzeros in registers, check them
-//    (span, and strictly increasing columns in each row, from a bitmask of
-//    row starts), publish the tile's description, then zero and fill the A
-//    window once the previous tile's MMAs have read it;
+//    (column span; no (row, column) pair twice, marked in a bitmask over the
+//    window), publish the tile's description, then zero and fill the A window
+//    once the previous tile's MMAs have read it;
 //  * warp 8 (producer) loads the B chunks of each tensor-core tile with TMA;
 //  * warp 9 (MMA) issues the MMAs once the A window and a B stage are full;
 //    tcgen05.commit frees the stage and the window and, per tile, marks the
@@ -39,8 +39,8 @@
 // kErrStageTimeout in the plan's error word and stops instead of hanging.
 //
 // A tile whose column span exceeds three chunks, one holding more than 8192
-// nonzeros, or one with a row whose columns do not strictly increase
-// (duplicates) is computed by the builders with per-row gathers; a tile with
+// nonzeros, or one with a duplicate (row, column) entry is computed by the
+// builders with per-row gathers (columns need not be sorted); a tile with
 // no nonzeros stores zero rows.  The dense product multiplies absent entries
 // as zeros, so a NaN/Inf in a B row inside the window reaches every row of
 // the tile; IEEE special values are outside the accepted inputs.
@@ -78,6 +78,10 @@ constexpr int kPerThread = 32;  // nonzeros a builder holds: a tile of at most 8
 constexpr int kTileNnz = kPerThread * kBuilders;
 enum TileKind { kTensor = 0, kZero = 1, kGather = 2 };
 constexpr int kTwFloats = 32 * 36;  // one epilogue warp's transpose buffer (rows of 36 floats)
+// Duplicate check: one bit per (row, window column); column k's 128 rows are
+// words 5k .. 5k+3 (a stride of 5 words puts 32 consecutive columns in 32
+// different banks).
+constexpr int kDupWords = kMaxChunks * kChunk * 5;
 // mbarriers: A full, A free, B full[3], B empty[3], accumulator full[2] and
 // drained[2], tile description full[2] and consumed[2]
 constexpr int kBars = 16;
@@ -87,8 +91,7 @@ __host__ __device__ constexpr size_t stage_bytes(int N) { return size_t(kBRows) 
 __host__ __device__ constexpr size_t smem_bytes(int N) {
   return size_t(kAWindow) + kStages * stage_bytes(N)  // A window, B stages
          + kTileNnz                                   // local row of every held nonzero (1 byte)
-         + (kBuilders / 32) * kPerThread * 4          // each builder warp's last-lane columns
-         + kTileNnz / 8                               // row-start bitmask over the held nonzeros
+         + kDupWords * 4                              // duplicate bitmask over the window
          + 4 * kTwFloats * 4                          // epilogue transposes
          + (kRows + 8) * 4                            // rowptr slice
          + kBars * 8 + 2 * 16 + 2 * 8 + 4 + 4 * 4 + 4;  // barriers, tile descriptions, ring, TMEM
@@ -205,9 +208,8 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
   unsigned char* s_A = smem;                                  // chunk c, term t at (3c + t) * kATile
   unsigned char* s_B = smem + kAWindow;                       // stage s at s * sb
   uint8_t* s_rowid = s_B + kStages * sb;                      // [kTileNnz] local row of each held nonzero
-  int* s_last = reinterpret_cast<int*>(s_rowid + kTileNnz);  // [8 warps][kPerThread] lane 31's columns
-  uint32_t* s_start = reinterpret_cast<uint32_t*>(s_last + (kBuilders / 32) * kPerThread);  // row-start bits
-  float* s_tw = reinterpret_cast<float*>(s_start + kTileNnz / 32);  // [4 warps][kTwFloats]
+  uint32_t* s_dup = reinterpret_cast<uint32_t*>(s_rowid + kTileNnz);  // [kDupWords] (row, column) bits
+  float* s_tw = reinterpret_cast<float*>(s_dup + kDupWords);          // [4 warps][kTwFloats]
   int* s_rp = reinterpret_cast<int*>(s_tw + 4 * kTwFloats);   // [kRows + 8] rowptr slice
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_rp + kRows + 8);
   int4* s_info = reinterpret_cast<int4*>(s_bar + kBars);      // [2] (first row, rows, cmin, kind | chunks << 8)
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
       const int nrows = min(kRows, M - i0);
       builders_sync();  // the previous tile is done with s_rp, s_red, s_rowid and s_last
       for (int t = tid; t <= nrows; t += kBuilders) s_rp[t] = ld_stream(rowptr + i0 + t, stream_pol);
-      s_start[tid] = 0u;  // kTileNnz / 32 == kBuilders words
+      for (int t = tid; t < kDupWords; t += kBuilders) s_dup[t] = 0u;
       if (tid == 0) {
         s_red[0] = INT_MAX;
         s_red[1] = -1;
@@ -301,55 +303,47 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         // the local row of every tile nonzero, one byte each (warp w fills rows w, w+8, ...)
         for (int r = w; r < nrows; r += kBuilders / 32)
           for (int g = s_rp[r] + lane; g < s_rp[r + 1]; g += 32) s_rowid[g - p0] = uint8_t(r);
-        // a bit per row start (an empty row starts nowhere)
-        for (int r = tid; r < nrows; r += kBuilders)
-          if (s_rp[r] < s_rp[r + 1]) {
-            const int pos = s_rp[r] - p0;
-            atomicOr(s_start + (pos >> 5), 1u << (pos & 31));
-          }
-        // lane 31's columns: the predecessors of the next warp's lane 0
-        if (lane == 31)
-#pragma unroll
-          for (int i = 0; i < kPerThread; ++i) s_last[w * kPerThread + i] = int(pk[i]);
       }
       builders_sync();
       if (fits) {
-        // span, and strictly increasing columns inside each row: a nonzero
-        // that does not start a row must exceed its predecessor g-1, which is
-        // lane-1's, the previous warp's lane 31's, or for thread 0 thread
-        // 255's of the previous round.  Nonzero p0 + tid + 256 i is bit
-        // `lane` of row-start word w + 8 i.
+        // column span, and the row of every held nonzero
         int lo = INT_MAX, hi = -1;
-        bool inc = true;
 #pragma unroll
         for (int i = 0; i < kPerThread; ++i) {
           const int g = p0 + tid + kBuilders * i;
-          const int c = int(pk[i]);
-          const int up = __shfl_up_sync(0xffffffffu, c, 1);
-          const uint32_t word = s_start[w + (kBuilders / 32) * i];
-          const int prev = lane > 0 ? up
-                                    : (w > 0 ? s_last[(w - 1) * kPerThread + i]
-                                             : s_last[(kBuilders / 32 - 1) * kPerThread + (i > 0 ? i - 1 : 0)]);
           const bool valid = g < p1;
-          const bool starts = (word >> lane) & 1u;
+          const int c = int(pk[i]);
           if (valid) {
             lo = min(lo, c);
             hi = max(hi, c);
           }
-          inc &= !valid || starts || c > prev;
           const int r = valid ? int(s_rowid[g - p0]) : 0;
           pk[i] = valid ? (uint32_t(r) << 16) | (uint32_t(c) & 0xFFFFu) : kNone;
         }
         lo = __reduce_min_sync(0xffffffffu, lo);
         hi = __reduce_max_sync(0xffffffffu, hi);
-        const bool all_inc = __all_sync(0xffffffffu, inc);
         if (lane == 0) {
           atomicMin(s_red + 0, lo);
           atomicMax(s_red + 1, hi);
-          if (!all_inc) atomicOr(s_red + 2, 1);
         }
       } else if (tid == 0) {
         s_red[2] = 1;  // too many nonzeros to hold: gather path
+      }
+      builders_sync();
+      if (fits && s_red[1] >= 0 && (s_red[1] - s_red[0]) / kChunk < kMaxChunks) {
+        // no (row, column) pair twice: each held nonzero sets its bit and
+        // looks at the bit's previous value
+        const int lo = s_red[0];
+        bool dup = false;
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i) {
+          if (pk[i] != kNone) {
+            const int k = int((pk[i] - uint32_t(lo)) & 0xFFFFu), r = int(pk[i] >> 16);
+            const uint32_t bit = 1u << (r & 31);
+            dup |= (atomicOr(s_dup + 5 * k + (r >> 5), bit) & bit) != 0;
+          }
+        }
+        if (__any_sync(0xffffffffu, dup) && lane == 0) atomicOr(s_red + 2, 1);
       }
       builders_sync();
       const int cmin = s_red[0], cmax = s_red[1];
