@@ -22,15 +22,15 @@
 // The kernel is persistent (one CTA per SM, tiles strided by the grid) and
 // its warps have four roles, so that the steps of consecutive tiles overlap:
 //
-//  * warps 0-7 (builders) hold a tile's nonzeros in registers, check them
+//  * warps 0-11 (builders) hold a tile's nonzeros in registers, check them
 //    (column span; no (row, column) pair twice, marked in a bitmask over the
 //    window), publish the tile's description, then zero and fill the A window
 //    once the previous tile's MMAs have read it;
-//  * warp 8 (producer) loads the B chunks of each tensor-core tile with TMA;
-//  * warp 9 (MMA) issues the MMAs once the A window and a B stage are full;
+//  * warp 12 (producer) loads the B pieces of each tensor-core tile with TMA;
+//  * warp 13 (MMA) issues the MMAs once the A window and a B stage are full;
 //    tcgen05.commit frees the stage and the window and, per tile, marks the
 //    accumulator full;
-//  * warps 10-13 (epilogue) read a full accumulator with tcgen05.ld (warp w
+//  * warps 14-17 (epilogue) read a full accumulator with tcgen05.ld (warp w
 //    reads lanes 32*(w%4)..), turn each 32 x 32 block around in shared memory
 //    so that every store writes 4 rows x 128 contiguous bytes, then mark the
 //    accumulator drained.
@@ -38,7 +38,7 @@
 // Every wait on an mbarrier is bounded: on expiry the kernel records
 // kErrStageTimeout in the plan's error word and stops instead of hanging.
 //
-// A tile whose column span exceeds three chunks, one holding more than 8192
+// A tile whose column span exceeds three chunks, one holding more than 8448
 // nonzeros, or one with a duplicate (row, column) entry is computed by the
 // builders with per-row gathers (columns need not be sorted); a tile with
 // no nonzeros stores zero rows.  The dense product multiplies absent entries
@@ -69,12 +69,12 @@ constexpr int kBMNStride = kBRows * 16;  // B: bytes between N-adjacent core mat
 constexpr int kStages = 3;
 constexpr int kATile = kRows * kChunk * 2;         // one bf16 term of one chunk: 16 KB
 constexpr int kAWindow = kMaxChunks * 3 * kATile;  // the whole window: 144 KB
-constexpr int kBuilders = 256;                     // builder threads (warps 0-7)
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kEpiWarp0 = 10;  // warps 10-13
-constexpr int kCtaThreads = 14 * 32;
-constexpr int kPerThread = 32;  // nonzeros a builder holds: a tile of at most 8192 uses the tensor cores
+constexpr int kBuilders = 384;                     // builder threads (warps 0-11)
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kEpiWarp0 = 14;  // warps 14-17
+constexpr int kCtaThreads = 18 * 32;
+constexpr int kPerThread = 22;  // nonzeros a builder holds: a tile of at most 8448 uses the tensor cores
 constexpr int kTileNnz = kPerThread * kBuilders;
 enum TileKind { kTensor = 0, kZero = 1, kGather = 2 };
 constexpr int kTwFloats = 32 * 36;  // one epilogue warp's transpose buffer (rows of 36 floats)
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
       builders_sync();
 
       // ---- the tile's nonzeros into registers (one load round) ----------
-      // Thread t holds nonzeros p0 + t + 256 i (i < kPerThread): its value and
+      // Thread t holds nonzeros p0 + t + 384 i (i < kPerThread): its value and
       // its column (later a packed word (row << 16) | local column), or kNone.
       const int p0 = s_rp[0], p1 = s_rp[nrows];
       const bool fits = p1 - p0 <= kTileNnz;
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         l2_prefetch(vals + q0, vals + q1);
       }
       if (fits) {
-        // the local row of every tile nonzero, one byte each (warp w fills rows w, w+8, ...)
+        // the local row of every tile nonzero, one byte each (warp w fills rows w, w+12, ...)
         for (int r = w; r < nrows; r += kBuilders / 32)
           for (int g = s_rp[r] + lane; g < s_rp[r + 1]; g += 32) s_rowid[g - p0] = uint8_t(r);
       }
