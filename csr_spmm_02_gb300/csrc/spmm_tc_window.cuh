@@ -93,7 +93,7 @@ __host__ __device__ constexpr size_t smem_bytes(int N) {
          + kTileNnz                                   // local row of every held nonzero (1 byte)
          + kDupWords * 4                              // duplicate bitmask over the window
          + 4 * kTwFloats * 4                          // epilogue transposes
-         + (kRows + 8) * 4                            // rowptr slice
+         + 2 * (kRows + 8) * 4                        // rowptr slices (this tile, the next)
          + kBars * 8 + 2 * 16 + 2 * 8 + 4 + 4 * 4 + 4;  // barriers, tile descriptions, ring, TMEM
                                                          // address, reductions, beat
 }
@@ -210,8 +210,8 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
   uint8_t* s_rowid = s_B + kStages * sb;                      // [kTileNnz] local row of each held nonzero
   uint32_t* s_dup = reinterpret_cast<uint32_t*>(s_rowid + kTileNnz);  // [kDupWords] (row, column) bits
   float* s_tw = reinterpret_cast<float*>(s_dup + kDupWords);          // [4 warps][kTwFloats]
-  int* s_rp = reinterpret_cast<int*>(s_tw + 4 * kTwFloats);   // [kRows + 8] rowptr slice
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_rp + kRows + 8);
+  int* s_rp_buf = reinterpret_cast<int*>(s_tw + 4 * kTwFloats);  // [2][kRows + 8] rowptr slices
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_rp_buf + 2 * (kRows + 8));
   int4* s_info = reinterpret_cast<int4*>(s_bar + kBars);      // [2] (first row, rows, cmin, kind | chunks << 8)
   int* s_ring = reinterpret_cast<int*>(s_info + 2);           // [2][2] first row and rows per accumulator
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ring + 4);
@@ -259,11 +259,16 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
     uint32_t tt = 0;  // tensor-core tiles built
     bool ok = true;
     int j = 0;
+    if (int(blockIdx.x) < ntiles) {  // the first tile's rowptr slice; each tile loads the next one's
+      const int i0 = blockIdx.x * kRows, nr = min(kRows, M - i0);
+      for (int t = tid; t <= nr; t += kBuilders) s_rp_buf[t] = ld_stream(rowptr + i0 + t, stream_pol);
+    }
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++j) {
       const int i0 = tile * kRows;
       const int nrows = min(kRows, M - i0);
-      builders_sync();  // the previous tile is done with s_rp, s_red, s_rowid and s_last
-      for (int t = tid; t <= nrows; t += kBuilders) s_rp[t] = ld_stream(rowptr + i0 + t, stream_pol);
+      int* s_rp = s_rp_buf + (j & 1) * (kRows + 8);
+      int* s_rp_next = s_rp_buf + ((j + 1) & 1) * (kRows + 8);
+      builders_sync();  // this tile's rowptr slice is in; the previous tile is done with s_red, s_rowid, s_dup
       for (int t = tid; t < kDupWords; t += kBuilders) s_dup[t] = 0u;
       if (tid == 0) {
         s_red[0] = INT_MAX;
@@ -271,8 +276,13 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         s_red[2] = 0;
         *s_beat = *s_beat + 1;
       }
-      // the next tile's nonzero range, for an L2 prefetch once this tile's loads are out
+      // the next tile's rowptr slice (stored at the end of this tile) and its
+      // nonzero range, for an L2 prefetch once this tile's loads are out
       const int next = tile + int(gridDim.x);
+      const int next_rows = next < ntiles ? min(kRows, M - next * kRows) : -1;
+      static_assert(kBuilders > kRows, "one rowptr entry per builder thread");
+      int rp_next = 0;
+      if (tid <= next_rows) rp_next = ld_stream(rowptr + int64_t(next) * kRows + tid, stream_pol);
       int q0 = 0, q1 = 0;
       if (tid == 32 && next < ntiles) {
         q0 = __ldg(rowptr + int64_t(next) * kRows);
@@ -357,6 +367,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         if (j >= 2) got = mbar_wait_bounded(bar(kInfoUsed + slot), (uint32_t(j >> 1) - 1) & 1u, kSpinLimit);
         s_info[slot] = make_int4(i0, nrows, cmin, kind | (nch << 8));
         mbar_arrive(bar(kInfoFull + slot));
+        if (kind == kTensor) l2_prefetch(B + size_t(cmin) * N, B + size_t(min(cmax + 1, K)) * N);  // for the TMA
       }
       if (!builders_and(got)) {
         ok = false;
@@ -423,6 +434,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
           }
         }
       }
+      if (tid <= next_rows) s_rp_next[tid] = rp_next;
     }
     if (!ok && tid == 0) atomicOr(err, kErrStageTimeout);
   } else if (w == kProducerWarp) {
