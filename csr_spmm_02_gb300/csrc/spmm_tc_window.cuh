@@ -26,7 +26,8 @@
 //    (column span; no (row, column) pair twice, marked in a bitmask over the
 //    window), publish the tile's description, then zero and fill the A window
 //    once the previous tile's MMAs have read it;
-//  * warp 12 (producer) loads the B pieces of each tensor-core tile with TMA;
+//  * warp 12 (producer) loads the B pieces of each tensor-core tile with TMA
+//    and prefetches the next tile's nonzeros into L2;
 //  * warp 13 (MMA) issues the MMAs once the A window and a B stage are full;
 //    tcgen05.commit frees the stage and the window and, per tile, marks the
 //    accumulator full;
@@ -276,18 +277,12 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         s_red[2] = 0;
         *s_beat = *s_beat + 1;
       }
-      // the next tile's rowptr slice (stored at the end of this tile) and its
-      // nonzero range, for an L2 prefetch once this tile's loads are out
+      // the next tile's rowptr slice, stored at the end of this tile
       const int next = tile + int(gridDim.x);
       const int next_rows = next < ntiles ? min(kRows, M - next * kRows) : -1;
       static_assert(kBuilders > kRows, "one rowptr entry per builder thread");
       int rp_next = 0;
       if (tid <= next_rows) rp_next = ld_stream(rowptr + int64_t(next) * kRows + tid, stream_pol);
-      int q0 = 0, q1 = 0;
-      if (tid == 32 && next < ntiles) {
-        q0 = __ldg(rowptr + int64_t(next) * kRows);
-        q1 = __ldg(rowptr + min(int64_t(M), int64_t(next) * kRows + kRows));
-      }
       builders_sync();
 
       // ---- the tile's nonzeros into registers (one load round) ----------
@@ -304,10 +299,6 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
           pk[i] = g < p1 ? uint32_t(ld_stream(colind + g, stream_pol)) : kNone;
           val[i] = g < p1 ? ld_stream(vals + g, stream_pol) : 0.f;
         }
-      }
-      if (tid == 32 && q1 > q0 && q1 - q0 <= kTileNnz) {
-        l2_prefetch(colind + q0, colind + q1);
-        l2_prefetch(vals + q0, vals + q1);
       }
       if (fits) {
         // the local row of every tile nonzero, one byte each (warp w fills rows w, w+12, ...)
@@ -451,6 +442,16 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         }
         const int4 info = s_info[slot];
         mbar_arrive(bar(kInfoUsed + slot));
+        // the next tile's nonzeros into L2 while the builders finish this one
+        const int next = tile + int(gridDim.x);
+        if (next < ntiles) {
+          const int q0 = __ldg(rowptr + int64_t(next) * kRows);
+          const int q1 = __ldg(rowptr + min(int64_t(M), int64_t(next) * kRows + kRows));
+          if (q1 > q0 && q1 - q0 <= kTileNnz) {
+            l2_prefetch(colind + q0, colind + q1);
+            l2_prefetch(vals + q0, vals + q1);
+          }
+        }
         if ((info.w & 0xFF) != kTensor) continue;
         const int pieces = (info.w >> 8) * (kChunk / kBRows);
         for (int c = 0; c < pieces; ++c) {
