@@ -20,6 +20,8 @@
 // many columns.  The summation order is fixed, so results are deterministic.
 #pragma once
 
+#include <algorithm>
+
 #include "spmm_device.cuh"
 #include "spmm_internal.h"
 
@@ -39,6 +41,21 @@ struct RowTiling {
   static constexpr int U = kU0 < kChunk ? kU0 : kChunk;  // nonzeros per batch; divides kChunk
 };
 
+// The group's pairs for staging slots [base, base + CH) of a row ending at
+// `end`: lane l holds slots base + l + G p (p < CH / G); slots past the end
+// hold (0, 0).
+template <int G, int PPL>
+__device__ __forceinline__ void load_pairs(int2 (&pr)[PPL], const int32_t* __restrict__ colind,
+                                           const float* __restrict__ vals, int base, int end, int lane,
+                                           uint64_t pol) {
+#pragma unroll
+  for (int p = 0; p < PPL; ++p) {
+    const int j = base + lane + G * p;
+    pr[p] = j < end ? make_int2(ld_stream(colind + j, pol), ld_stream(reinterpret_cast<const int*>(vals) + j, pol))
+                    : make_int2(0, 0);
+  }
+}
+
 template <typename BT, int VEC, int G, int NCH>
 __global__ void __launch_bounds__(kThreads, SPMM_ROW_MIN_BLOCKS)
     spmm_row_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr,
@@ -47,11 +64,17 @@ __global__ void __launch_bounds__(kThreads, SPMM_ROW_MIN_BLOCKS)
   constexpr int kGroups = kThreads / G;
   constexpr int CH = RowTiling<G, NCH>::kChunk;
   constexpr int U = RowTiling<G, NCH>::U;
+  constexpr int PPL = CH / G;  // staged pairs per lane
   __shared__ int2 s_cv[kGroups * CH];  // group g stages (col, val bits) in s_cv[g*CH, g*CH+CH)
 
   const int lane = threadIdx.x & (G - 1);
   const int grp = threadIdx.x / G;
-  const int64_t row = int64_t(blockIdx.x) * kGroups + grp;
+  // Persistent: group g of CTA b takes rows b*kGroups + g, then every
+  // gridDim.x*kGroups rows further.  The next row's bounds and first pairs
+  // are loaded while the current row's gathers run, so a row's chain is its
+  // gathers alone.
+  const int64_t stride = int64_t(gridDim.x) * kGroups;
+  int64_t row = int64_t(blockIdx.x) * kGroups + grp;
   if (row >= M) return;  // the whole group leaves together
   const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << ((threadIdx.x & 31) & ~(G - 1)));
   int2* cv = s_cv + grp * CH;
@@ -67,71 +90,109 @@ __global__ void __launch_bounds__(kThreads, SPMM_ROW_MIN_BLOCKS)
     coff[ch] = col0 + (ch * G + lane) * VEC;
     bl[ch] = B + min(coff[ch], N - VEC);
   }
-  FVec<VEC> acc[NCH];
-#pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) acc[ch].zero();
 
   const uint64_t stream_pol = policy_evict_first();
-  const int start = ld_stream(rowptr + row, stream_pol);
-  const int end = ld_stream(rowptr + row + 1, stream_pol);
-  for (int base = start; base < end; base += CH) {
-    const int cnt = min(CH, end - base);
-    __syncwarp(gmask);  // every lane has finished with the previous chunk
-    for (int j = lane; j < cnt; j += G)
-      cv[j] = make_int2(ld_stream(colind + base + j, stream_pol),
-                        ld_stream(reinterpret_cast<const int*>(vals) + base + j, stream_pol));
-    __syncwarp(gmask);
-    int t = 0;
-    for (; t + U <= cnt; t += U) {  // full batches: gathers first, then the FMAs
-      BSlice<BT, VEC> bs[U][NCH];
+  int start = ld_stream(rowptr + row, stream_pol);
+  int end = ld_stream(rowptr + row + 1, stream_pol);
+  int2 pr[PPL];
+  load_pairs<G, PPL>(pr, colind, vals, start, end, lane, stream_pol);
+  for (; row < M; row += stride) {
+    const int64_t nrow = row + stride;
+    int nstart = 0, nend = 0;
+    if (nrow < M) {
+      nstart = ld_stream(rowptr + nrow, stream_pol);
+      nend = ld_stream(rowptr + nrow + 1, stream_pol);
+    }
+    FVec<VEC> acc[NCH];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const size_t roff = size_t(cv[t + u].x) * N;
+    for (int ch = 0; ch < NCH; ++ch) acc[ch].zero();
+    for (int base = start; base < end; base += CH) {
+      const int cnt = min(CH, end - base);
+      __syncwarp(gmask);  // every lane has finished with the previous chunk
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(bl[ch] + roff);
+      for (int p = 0; p < PPL; ++p) cv[lane + G * p] = pr[p];
+      __syncwarp(gmask);
+      // the pairs of the next chunk, or of the next row's first chunk
+      if (base + CH < end) load_pairs<G, PPL>(pr, colind, vals, base + CH, end, lane, stream_pol);
+      else load_pairs<G, PPL>(pr, colind, vals, nstart, nend, lane, stream_pol);
+      int t = 0;
+      for (; t + U <= cnt; t += U) {  // full batches: gathers first, then the FMAs
+        BSlice<BT, VEC> bs[U][NCH];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const size_t roff = size_t(cv[t + u].x) * N;
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(bl[ch] + roff);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float2 vv = pair(__int_as_float(cv[t + u].y));  // re-read: frees registers
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) {
+            FVec<VEC> b;
+            bs[u][ch].widen(b);
+            acc[ch].fma(vv, b);
+          }
+        }
       }
+      if (t < cnt) {  // short last batch: padded slots re-read the last row with value 0
+        BSlice<BT, VEC> bs[U][NCH];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const float2 vv = pair(__int_as_float(cv[t + u].y));  // re-read: frees registers
+        for (int u = 0; u < U; ++u) {
+          const size_t roff = size_t(cv[min(t + u, cnt - 1)].x) * N;
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          FVec<VEC> b;
-          bs[u][ch].widen(b);
-          acc[ch].fma(vv, b);
+          for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(bl[ch] + roff);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float2 vv = pair(t + u < cnt ? __int_as_float(cv[t + u].y) : 0.f);
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) {
+            FVec<VEC> b;
+            bs[u][ch].widen(b);
+            acc[ch].fma(vv, b);
+          }
         }
       }
     }
-    if (t < cnt) {  // short last batch: padded slots re-read the last row with value 0
-      BSlice<BT, VEC> bs[U][NCH];
+    if (start == end) load_pairs<G, PPL>(pr, colind, vals, nstart, nend, lane, stream_pol);  // empty row
+    float* crow = C + size_t(row) * N;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const size_t roff = size_t(cv[min(t + u, cnt - 1)].x) * N;
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(bl[ch] + roff);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const float2 vv = pair(t + u < cnt ? __int_as_float(cv[t + u].y) : 0.f);
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          FVec<VEC> b;
-          bs[u][ch].widen(b);
-          acc[ch].fma(vv, b);
-        }
-      }
-    }
+    for (int ch = 0; ch < NCH; ++ch)
+      if (coff[ch] < N) store_c<VEC>(crow + coff[ch], acc[ch]);
+    start = nstart;
+    end = nend;
   }
-  float* crow = C + size_t(row) * N;
-#pragma unroll
-  for (int ch = 0; ch < NCH; ++ch)
-    if (coff[ch] < N) store_c<VEC>(crow + coff[ch], acc[ch]);
+}
+
+// Resident CTAs per SM of one instantiation, looked up once per device.
+template <typename BT, int VEC, int G, int NCH>
+int row_blocks_per_sm(int dev) {
+  static int cached[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  if (!cached[dev]) {
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, spmm_row_kernel<BT, VEC, G, NCH>, kThreads, 0) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 1;
+    cached[dev] = std::max(1, per_sm) * std::max(1, sms);
+  }
+  return cached[dev];
 }
 
 template <typename BT, int VEC, int G, int NCH>
 cudaError_t launch_row_t(const Launch& L) {
   constexpr int kGroups = kThreads / G;
   constexpr int TW = G * VEC * NCH;
-  const dim3 grid(unsigned((int64_t(L.M) + kGroups - 1) / kGroups), unsigned((L.N + TW - 1) / TW));
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned tiles = unsigned((L.N + TW - 1) / TW);
+  // one wave of resident CTAs over all column tiles
+  const int64_t need = (int64_t(L.M) + kGroups - 1) / kGroups;
+  const int64_t wave = std::max<int64_t>(1, row_blocks_per_sm<BT, VEC, G, NCH>(dev) / int64_t(tiles));
+  const dim3 grid(unsigned(std::min(need, wave)), tiles);
   spmm_row_kernel<BT, VEC, G, NCH><<<grid, kThreads, 0, L.stream>>>(
       L.M, L.N, L.rowptr, L.colind, L.vals, static_cast<const BT*>(L.B), L.C);
   return cudaGetLastError();
