@@ -41,6 +41,28 @@ struct RowTiling {
   static constexpr int U = kU0 < kChunk ? kU0 : kChunk;  // nonzeros per batch; divides kChunk
 };
 
+// B-slice loads of the row kernel with an L2 policy: B rows get evict-last
+// priority, since every B row is gathered again by other rows (the bytes
+// loaded are those of BSlice::load).
+__device__ __forceinline__ uint4 ld_b16_policy(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void gather_keep(BSlice<float, 4>& s, const float* p, uint64_t pol) {
+  const uint4 v = ld_b16_policy(p, pol);
+  s.r = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
+__device__ __forceinline__ void gather_keep(BSlice<uint16_t, 8>& s, const uint16_t* p, uint64_t pol) {
+  s.r = ld_b16_policy(p, pol);
+}
+template <typename BT>
+__device__ __forceinline__ void gather_keep(BSlice<BT, 1>& s, const BT* p, uint64_t) {  // scalar path
+  s.load(p);
+}
+
 // The group's pairs for staging slots [base, base + CH) of a row ending at
 // `end`: lane l holds slots base + l + G p (p < CH / G); slots past the end
 // hold (0, 0).
@@ -92,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, SPMM_ROW_MIN_BLOCKS)
   }
 
   const uint64_t stream_pol = policy_evict_first();
+  const uint64_t keep_pol = policy_evict_last();  // B rows: reused by many rows
   int start = ld_stream(rowptr + row, stream_pol);
   int end = ld_stream(rowptr + row + 1, stream_pol);
   int2 pr[PPL];
@@ -122,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, SPMM_ROW_MIN_BLOCKS)
         for (int u = 0; u < U; ++u) {
           const size_t roff = size_t(cv[t + u].x) * N;
 #pragma unroll
-          for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(bl[ch] + roff);
+          for (int ch = 0; ch < NCH; ++ch) gather_keep(bs[u][ch], bl[ch] + roff, keep_pol);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -141,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, SPMM_ROW_MIN_BLOCKS)
         for (int u = 0; u < U; ++u) {
           const size_t roff = size_t(cv[min(t + u, cnt - 1)].x) * N;
 #pragma unroll
-          for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(bl[ch] + roff);
+          for (int ch = 0; ch < NCH; ++ch) gather_keep(bs[u][ch], bl[ch] + roff, keep_pol);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
