@@ -64,7 +64,6 @@ constexpr int kRows = 128;       // rows per tile = MMA M
 constexpr int kChunk = 64;       // window columns per chunk (4 K-steps of 16)
 constexpr int kMaxChunks = 3;    // larger spans use the gather path
 constexpr int kKStride = 128;    // bytes between K-adjacent core matrices (8 rows x 16 bytes)
-constexpr int kMNStride = 1024;  // A: bytes between M-adjacent core matrices (8 along K per chunk)
 constexpr int kBRows = 32;       // B rows per stage (2 K-steps)
 constexpr int kBMNStride = kBRows * 16;  // B: bytes between N-adjacent core matrices
 constexpr int kStages = 3;
@@ -110,6 +109,24 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
   d |= uint64_t(1) << 46;  // descriptor version of this architecture
   return d;                // base offset 0, layout type 0 (no swizzle)
+}
+
+// The A tiles use the K-major 128-byte swizzled layout instead: row r of a
+// tile is the 128 bytes at r * 128 (its 64 K-elements), 8-row groups 1024
+// bytes apart, and 16-byte piece c of a row sits at piece c ^ (r & 7).  A
+// warp's consecutive nonzeros of one row then fall in distinct banks.  The
+// tile base is 1024-byte aligned and a K-step of 16 advances the start
+// address by 32 bytes (the swizzle acts on the address bits).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(1) << 16;             // leading-byte offset: unused for swizzled K-major
+  d |= uint64_t(1024 >> 4) << 32;     // stride-byte offset: 8-row groups
+  d |= uint64_t(1) << 46;             // descriptor version of this architecture
+  d |= uint64_t(2) << 61;             // layout type: 128-byte swizzle
+  return d;
+}
+__device__ __forceinline__ uint32_t a_offset(int r, int kk) {  // byte of element (r, kk) in a tile
+  return uint32_t(r) * 128u + (uint32_t((kk >> 3) ^ (r & 7)) << 4) + uint32_t(kk & 7) * 2u;
 }
 
 // kind::f16 instruction descriptor: D fp32, A and B bf16, A K-major, B
@@ -390,8 +407,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
             const float r1 = v - bf16_bits_to_float(h);
             const uint16_t m = bf16_rn_bits(r1);
             const uint16_t l = bf16_rn_bits(r1 - bf16_bits_to_float(m));
-            const uint32_t off = uint32_t(3 * ch) * kATile + uint32_t(r >> 3) * kMNStride +
-                                 uint32_t(kk >> 3) * kKStride + uint32_t(r & 7) * 16 + uint32_t(kk & 7) * 2;
+            const uint32_t off = uint32_t(3 * ch) * kATile + a_offset(r, kk);
             *reinterpret_cast<uint16_t*>(s_A + off) = h;
             *reinterpret_cast<uint16_t*>(s_A + kATile + off) = m;
             *reinterpret_cast<uint16_t*>(s_A + 2 * kATile + off) = l;
@@ -509,9 +525,8 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
           for (int ks = 0; ks < kBRows / 16; ++ks) {
 #pragma unroll
             for (int term = 0; term < 3; ++term) {
-              const uint64_t a = sdesc(a_base + uint32_t(3 * ch + term) * kATile +
-                                           uint32_t(2 * (kp * (kBRows / 16) + ks)) * kKStride,
-                                       kKStride, kMNStride);
+              const uint64_t a = sdesc_sw128(a_base + uint32_t(3 * ch + term) * kATile +
+                                             uint32_t(kp * (kBRows / 16) + ks) * 32u);
               const uint64_t bd = sdesc(b_base + s * uint32_t(sb) + uint32_t(2 * ks) * kKStride, kKStride, kBMNStride);
               mma(acc, a, bd, id, c > 0 || ks > 0 || term > 0);
             }
