@@ -22,10 +22,12 @@
 // The kernel is persistent (one CTA per SM, tiles strided by the grid) and
 // its warps have four roles, so that the steps of consecutive tiles overlap:
 //
-//  * warps 0-11 (builders) hold a tile's nonzeros in registers, check them
-//    (column span; no (row, column) pair twice, marked in a bitmask over the
-//    window), publish the tile's description, then zero and fill the A window
-//    once the previous tile's MMAs have read it;
+//  * warps 0-11 (builders) hold a tile's nonzeros in registers, check the
+//    column span, publish the tile's description, then zero and fill the A
+//    window once the previous tile's MMAs have read it; the hi terms go in
+//    with shared-memory atomicOr, whose old value shows a (row, column) pair
+//    met twice (a tile with such duplicates is discarded by the epilogue and
+//    gathered by the builders instead);
 //  * warp 12 (producer) loads the B pieces of each tensor-core tile with TMA
 //    and prefetches the next tile's nonzeros into L2;
 //  * warp 13 (MMA) issues the MMAs once the A window and a B stage are full;
@@ -40,8 +42,9 @@
 // kErrStageTimeout in the plan's error word and stops instead of hanging.
 //
 // A tile whose column span exceeds three chunks, one holding more than 8448
-// nonzeros, or one with a duplicate (row, column) entry is computed by the
-// builders with per-row gathers (columns need not be sorted); a tile with
+// nonzeros, or one with a duplicate (row, column) entry (both nonzero) is
+// computed by the builders with per-row gathers (columns need not be
+// sorted); a tile with
 // no nonzeros stores zero rows.  The dense product multiplies absent entries
 // as zeros, so a NaN/Inf in a B row inside the window reaches every row of
 // the tile; IEEE special values are outside the accepted inputs.
@@ -78,10 +81,6 @@ constexpr int kPerThread = 22;  // nonzeros a builder holds: a tile of at most 8
 constexpr int kTileNnz = kPerThread * kBuilders;
 enum TileKind { kTensor = 0, kZero = 1, kGather = 2 };
 constexpr int kTwFloats = 32 * 36;  // one epilogue warp's transpose buffer (rows of 36 floats)
-// Duplicate check: one bit per (row, window column); column k's 128 rows are
-// words 5k .. 5k+3 (a stride of 5 words puts 32 consecutive columns in 32
-// different banks).
-constexpr int kDupWords = kMaxChunks * kChunk * 5;
 // mbarriers: A full, A free, B full[3], B empty[3], accumulator full[2] and
 // drained[2], tile description full[2] and consumed[2]
 constexpr int kBars = 16;
@@ -91,7 +90,6 @@ __host__ __device__ constexpr size_t stage_bytes(int N) { return size_t(kBRows) 
 __host__ __device__ constexpr size_t smem_bytes(int N) {
   return size_t(kAWindow) + kStages * stage_bytes(N)  // A window, B stages
          + kTileNnz                                   // local row of every held nonzero (1 byte)
-         + kDupWords * 4                              // duplicate bitmask over the window
          + 4 * kTwFloats * 4                          // epilogue transposes
          + 2 * (kRows + 8) * 4                        // rowptr slices (this tile, the next)
          + kBars * 8 + 2 * 16 + 2 * 8 + 4 + 4 * 4 + 4;  // barriers, tile descriptions, ring, TMEM
@@ -192,6 +190,18 @@ __device__ __forceinline__ bool builders_and(bool p) {
   return r != 0;
 }
 
+// The same barrier, returning whether `p` holds in some builder thread.
+__device__ __forceinline__ bool builders_or(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.or.pred b, 1, %2, a;\n\tselp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(p)), "n"(kBuilders)
+      : "memory");
+  return r != 0;
+}
+
 // Bounded wait that tolerates slow builders: the poll budget restarts while
 // `beat` (advanced by the builders per tile and per gathered row) moves, so it
 // expires only when the builders make no progress.
@@ -226,14 +236,13 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
   unsigned char* s_A = smem;                                  // chunk c, term t at (3c + t) * kATile
   unsigned char* s_B = smem + kAWindow;                       // stage s at s * sb
   uint8_t* s_rowid = s_B + kStages * sb;                      // [kTileNnz] local row of each held nonzero
-  uint32_t* s_dup = reinterpret_cast<uint32_t*>(s_rowid + kTileNnz);  // [kDupWords] (row, column) bits
-  float* s_tw = reinterpret_cast<float*>(s_dup + kDupWords);          // [4 warps][kTwFloats]
+  float* s_tw = reinterpret_cast<float*>(s_rowid + kTileNnz);  // [4 warps][kTwFloats]
   int* s_rp_buf = reinterpret_cast<int*>(s_tw + 4 * kTwFloats);  // [2][kRows + 8] rowptr slices
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_rp_buf + 2 * (kRows + 8));
   int4* s_info = reinterpret_cast<int4*>(s_bar + kBars);      // [2] (first row, rows, cmin, kind | chunks << 8)
   int* s_ring = reinterpret_cast<int*>(s_info + 2);           // [2][2] first row and rows per accumulator
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_ring + 4);
-  int* s_red = reinterpret_cast<int*>(s_tmem + 1);            // [0] min col, [1] max col, [2] flags
+  int* s_red = reinterpret_cast<int*>(s_tmem + 1);  // [0] min col, [1] max col, [2] flags, [3] discard
   volatile int* s_beat = s_red + 4;                           // builders' progress counter
 
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -286,8 +295,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
       const int nrows = min(kRows, M - i0);
       int* s_rp = s_rp_buf + (j & 1) * (kRows + 8);
       int* s_rp_next = s_rp_buf + ((j + 1) & 1) * (kRows + 8);
-      builders_sync();  // this tile's rowptr slice is in; the previous tile is done with s_red, s_rowid, s_dup
-      for (int t = tid; t < kDupWords; t += kBuilders) s_dup[t] = 0u;
+      builders_sync();  // this tile's rowptr slice is in; the previous tile is done with s_red and s_rowid
       if (tid == 0) {
         s_red[0] = INT_MAX;
         s_red[1] = -1;
@@ -348,22 +356,6 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         s_red[2] = 1;  // too many nonzeros to hold: gather path
       }
       builders_sync();
-      if (fits && s_red[1] >= 0 && (s_red[1] - s_red[0]) / kChunk < kMaxChunks) {
-        // no (row, column) pair twice: each held nonzero sets its bit and
-        // looks at the bit's previous value
-        const int lo = s_red[0];
-        bool dup = false;
-#pragma unroll
-        for (int i = 0; i < kPerThread; ++i) {
-          if (pk[i] != kNone) {
-            const int k = int((pk[i] - uint32_t(lo)) & 0xFFFFu), r = int(pk[i] >> 16);
-            const uint32_t bit = 1u << (r & 31);
-            dup |= (atomicOr(s_dup + 5 * k + (r >> 5), bit) & bit) != 0;
-          }
-        }
-        if (__any_sync(0xffffffffu, dup) && lane == 0) atomicOr(s_red + 2, 1);
-      }
-      builders_sync();
       const int cmin = s_red[0], cmax = s_red[1];
       const int nch = cmax < 0 ? 0 : (cmax - cmin) / kChunk + 1;
       const int kind = (s_red[2] != 0 || nch > kMaxChunks) ? kGather : (nch == 0 ? kZero : kTensor);
@@ -382,6 +374,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         break;
       }
 
+      bool discard = false;  // a tensor-core tile with duplicate entries
       if (kind == kTensor) {
         // local column of each held nonzero: its low 16 bits minus cmin's,
         // modulo 2^16 (exact, since the span is below 2^16)
@@ -396,7 +389,11 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         for (int t = tid; t < nch * 3 * kATile / 16; t += kBuilders)
           reinterpret_cast<uint4*>(s_A)[t] = make_uint4(0u, 0u, 0u, 0u);
         builders_sync();
-        // every held nonzero into its chunk: value -> three bf16 terms
+        // every held nonzero into its chunk: value -> three bf16 terms.  A
+        // zero value adds nothing and is left out; the hi term of any other
+        // value is nonzero, so an atomicOr that finds its half-word already
+        // set has met a second nonzero for the same (row, column).
+        bool dup = false;
 #pragma unroll
         for (int i = 0; i < kPerThread; ++i) {
           if (pk[i] != kNone) {
@@ -404,25 +401,33 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
             const int ch = k >> 6, kk = k & (kChunk - 1);
             const float v = val[i];
             const uint16_t h = bf16_rn_bits(v);
-            const float r1 = v - bf16_bits_to_float(h);
-            const uint16_t m = bf16_rn_bits(r1);
-            const uint16_t l = bf16_rn_bits(r1 - bf16_bits_to_float(m));
-            const uint32_t off = uint32_t(3 * ch) * kATile + a_offset(r, kk);
-            *reinterpret_cast<uint16_t*>(s_A + off) = h;
-            *reinterpret_cast<uint16_t*>(s_A + kATile + off) = m;
-            *reinterpret_cast<uint16_t*>(s_A + 2 * kATile + off) = l;
+            if (h != 0) {
+              const float r1 = v - bf16_bits_to_float(h);
+              const uint16_t m = bf16_rn_bits(r1);
+              const uint16_t l = bf16_rn_bits(r1 - bf16_bits_to_float(m));
+              const uint32_t off = uint32_t(3 * ch) * kATile + a_offset(r, kk);
+              const uint32_t shift = (off & 2u) * 8u;
+              const uint32_t old = atomicOr(reinterpret_cast<uint32_t*>(s_A + (off & ~3u)), uint32_t(h) << shift);
+              dup |= ((old >> shift) & 0xFFFFu) != 0;
+              *reinterpret_cast<uint16_t*>(s_A + kATile + off) = m;
+              *reinterpret_cast<uint16_t*>(s_A + 2 * kATile + off) = l;
+            }
           }
         }
         fence_proxy_async();  // generic-proxy writes become visible to the tensor cores
-        builders_sync();
-        if (tid == 0) mbar_arrive(bar(kAFull));
+        discard = builders_or(dup);
+        if (tid == 0) {
+          s_red[3] = discard;  // read by the MMA warp once the window is full
+          mbar_arrive(bar(kAFull));
+        }
         ++tt;
-      } else if (kind == kZero) {  // no nonzeros in the tile: zero rows
+      }
+      if (kind == kZero) {  // no nonzeros in the tile: zero rows
         for (int t = tid; t < nrows * (N / 4); t += kBuilders) {
           const int r = t / (N / 4), c4 = t - r * (N / 4);
           st_stream4(C + size_t(i0 + r) * N + 4 * c4, 0.f, 0.f, 0.f, 0.f);
         }
-      } else {  // gather path: warp w computes rows w, w + 8, ... (8 columns per lane per pass)
+      } else if (kind == kGather || discard) {  // gather path: warp w computes rows w, w + 12, ...
         for (int r = w; r < nrows; r += kBuilders / 32) {
           const int start = s_rp[r], end = s_rp[r + 1];
           if (tid == 0) *s_beat = *s_beat + 1;
@@ -511,6 +516,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
           break;
         }
         fence_after();
+        const bool discard = s_red[3] != 0;  // written by the builders before the window-full arrive
         const uint32_t acc = tmem + b * acc_cols;
         // piece c holds B rows cmin + 32c ..: K-steps 2c, 2c+1 of the window
         for (int c = 0; c < nch * (kChunk / kBRows) && ok; ++c) {
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         if (!ok) break;
         commit(bar(kAFree));  // the window too
         s_ring[2 * b] = info.x;
-        s_ring[2 * b + 1] = info.y;
+        s_ring[2 * b + 1] = discard ? 0 : info.y;  // a discarded tile is gathered by the builders
         commit(bar(kAccFull + b));  // the accumulator is complete once the MMAs are
         mbar_arrive(bar(kAccFull + b));
         ++tt;
