@@ -68,7 +68,8 @@ constexpr int kChunk = 64;       // window columns per chunk (4 K-steps of 16)
 constexpr int kMaxChunks = 3;    // larger spans use the gather path
 constexpr int kKStride = 128;    // bytes between K-adjacent core matrices (8 rows x 16 bytes)
 constexpr int kBRows = 32;       // B rows per stage (2 K-steps)
-constexpr int kBMNStride = kBRows * 16;  // B: bytes between N-adjacent core matrices
+constexpr int kBCols = 64;                // B columns per TMA box (128 bytes: one swizzle span)
+constexpr int kBBox = kBRows * kBCols * 2;  // one box: 32 rows x 128 bytes = 4 KB
 constexpr int kStages = 3;
 constexpr int kATile = kRows * kChunk * 2;         // one bf16 term of one chunk: 16 KB
 constexpr int kAWindow = kMaxChunks * 3 * kATile;  // the whole window: 144 KB
@@ -85,7 +86,7 @@ constexpr int kTwFloats = 32 * 36;  // one epilogue warp's transpose buffer (row
 // drained[2], tile description full[2] and consumed[2]
 constexpr int kBars = 16;
 
-__host__ __device__ constexpr size_t stage_bytes(int N) { return size_t(kBRows) * N * 2; }
+__host__ __device__ constexpr size_t stage_bytes(int N) { return size_t((N + kBCols - 1) / kBCols) * kBBox; }
 
 __host__ __device__ constexpr size_t smem_bytes(int N) {
   return size_t(kAWindow) + kStages * stage_bytes(N)  // A window, B stages
@@ -119,6 +120,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
   d |= uint64_t(1) << 16;             // leading-byte offset: unused for swizzled K-major
   d |= uint64_t(1024 >> 4) << 32;     // stride-byte offset: 8-row groups
+  d |= uint64_t(1) << 46;             // descriptor version of this architecture
+  d |= uint64_t(2) << 61;             // layout type: 128-byte swizzle
+  return d;
+}
+// B pieces are MN-major with the same 128-byte swizzle, as the TMA unit lays
+// them out: K-row k of a 64-column block is the 128 bytes at k * 128 (16-byte
+// piece c at c ^ (k & 7)), 8-row groups 1024 bytes apart along K, 64-column
+// blocks 4 KB apart along N.  A K-step of 16 rows advances the start by 2 KB.
+__device__ __forceinline__ uint64_t sdesc_b_sw128(uint32_t saddr) {
+  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(kBBox >> 4) << 16;    // leading-byte offset: next 64-column block (N)
+  d |= uint64_t(1024 >> 4) << 32;     // stride-byte offset: next 8 rows (K)
   d |= uint64_t(1) << 46;             // descriptor version of this architecture
   d |= uint64_t(2) << 61;             // layout type: 128-byte swizzle
   return d;
@@ -166,8 +179,9 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// One 2-D TMA box of B (8 columns x 32 rows, 512 bytes) into shared memory,
-// completing its bytes on `bar`.  x (the column) is a multiple of 8.
+// One 2-D TMA box of B (64 columns x 32 rows, 4 KB, 128-byte swizzled) into
+// shared memory, completing its bytes on `bar`.  x (the column) is a
+// multiple of 64.
 __device__ __forceinline__ void tma_load_b(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
@@ -483,8 +497,8 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
           }
           mbar_arrive_expect_tx(bar(kBFull + s), uint32_t(sb));
           const uint32_t dst = smem_addr(s_B + s * sb);
-          for (int q = 0; q < N / 8; ++q)
-            tma_load_b(dst + uint32_t(q) * kBMNStride, &bmap, 8 * q, info.z + c * kBRows, bar(kBFull + s));
+          for (int q = 0; q < (N + kBCols - 1) / kBCols; ++q)
+            tma_load_b(dst + uint32_t(q) * kBBox, &bmap, kBCols * q, info.z + c * kBRows, bar(kBFull + s));
           ++gc;
         }
       }
@@ -533,7 +547,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
             for (int term = 0; term < 3; ++term) {
               const uint64_t a = sdesc_sw128(a_base + uint32_t(3 * ch + term) * kATile +
                                              uint32_t(kp * (kBRows / 16) + ks) * 32u);
-              const uint64_t bd = sdesc(b_base + s * uint32_t(sb) + uint32_t(2 * ks) * kKStride, kKStride, kBMNStride);
+              const uint64_t bd = sdesc_b_sw128(b_base + s * uint32_t(sb) + uint32_t(ks) * 2048u);
               mma(acc, a, bd, id, c > 0 || ks > 0 || term > 0);
             }
           }
@@ -634,16 +648,16 @@ inline EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// B (K x N bf16, row-major) as a 2-D tensor for TMA: boxes of 8 columns x 32 rows.
+// B (K x N bf16, row-major) as a 2-D tensor for TMA: boxes of 64 columns x 32 rows, 128-byte swizzle.
 inline cudaError_t make_b_map(const uint16_t* B, int32_t K, int32_t N, CUtensorMap* map) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(K)};
   const cuuint64_t strides[1] = {cuuint64_t(N) * 2};
-  const cuuint32_t box[2] = {8, uint32_t(tc::kBRows)};
+  const cuuint32_t box[2] = {uint32_t(tc::kBCols), uint32_t(tc::kBRows)};
   const cuuint32_t elem[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(B), dims, strides, box, elem,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorNotSupported;
 }
