@@ -12,10 +12,11 @@
 //    fp32, so three MMAs per K-step reproduce the fp32 products and only the
 //    accumulation order differs from a row loop;
 //  * the tile's window (at most three chunks of 64 columns) is built once in
-//    shared memory as three K-major bf16 tiles per chunk; B is streamed in
-//    32-row pieces by the tensor memory accelerator (one 32 x 8 box per 16
-//    bytes of row, landing directly in the MN-major core-matrix layout, rows
-//    past K zero-filled) through three stages;
+//    shared memory as three K-major bf16 tiles per chunk (128-byte swizzled
+//    layout); B is streamed in 32-row pieces by the tensor memory accelerator
+//    (boxes of 64 columns x 32 rows, 128-byte swizzled, landing directly in the
+//    MN-major layout the MMA reads; rows past K zero-filled) through three
+//    stages;
 //  * per chunk, 4 K-steps x 3 terms of M=128, N, K=16 MMAs accumulate into one
 //    of two tensor-memory accumulators.
 //
@@ -66,7 +67,6 @@ namespace tc {
 constexpr int kRows = 128;       // rows per tile = MMA M
 constexpr int kChunk = 64;       // window columns per chunk (4 K-steps of 16)
 constexpr int kMaxChunks = 3;    // larger spans use the gather path
-constexpr int kKStride = 128;    // bytes between K-adjacent core matrices (8 rows x 16 bytes)
 constexpr int kBRows = 32;       // B rows per stage (2 K-steps)
 constexpr int kBCols = 64;                // B columns per TMA box (128 bytes: one swizzle span)
 constexpr int kBBox = kBRows * kBCols * 2;  // one box: 32 rows x 128 bytes = 4 KB
@@ -97,20 +97,12 @@ __host__ __device__ constexpr size_t smem_bytes(int N) {
                                                          // address, reductions, beat
 }
 
-// Shared-memory matrix descriptor: no swizzle, canonical core-matrix layout
-// (8 rows x 16 bytes per core matrix).  For the K-major A and the MN-major B
-// alike, the leading-byte-offset field holds the stride between K-adjacent core
-// matrices and the stride-byte-offset field the stride between M/N-adjacent
-// ones (the other assignments give wrong products on exact integer inputs).
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
-  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
-  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
-  d |= uint64_t(1) << 46;  // descriptor version of this architecture
-  return d;                // base offset 0, layout type 0 (no swizzle)
-}
-
-// The A tiles use the K-major 128-byte swizzled layout instead: row r of a
+// Shared-memory matrix descriptors (tcgen05): start address >> 4 in bits
+// 0-13, leading-byte offset >> 4 in 16-29, stride-byte offset >> 4 in 32-45,
+// version 1 in 46-47, layout type in 61-63.  Both operands use the 128-byte
+// swizzle; the field assignments below were checked on exact integer inputs.
+//
+// A tiles use the K-major 128-byte swizzled layout: row r of a
 // tile is the 128 bytes at r * 128 (its 64 K-elements), 8-row groups 1024
 // bytes apart, and 16-byte piece c of a row sits at piece c ^ (r & 7).  A
 // warp's consecutive nonzeros of one row then fall in distinct banks.  The

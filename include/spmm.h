@@ -102,7 +102,11 @@ typedef enum {
                               * 128-row tiles, A's fp32 values split exactly into three
                               * bf16 terms, B streamed by TMA in 64-row chunks; tiles
                               * with a span over 192 columns or duplicate columns gather
-                              * per row.  Other B types or widths run the window kernel. */
+                              * per row.  Other B types or widths run the window kernel.
+                              * The three-term split is exact for |vals| >= 2^-110;
+                              * smaller values keep fewer bits (under about 2^-134 they
+                              * are dropped), which can exceed the tolerance for a row
+                              * dominated by such values. */
 } spmm_kernel;
 
 /* Opaque plan: owns its device workspace (merge-path partition, carry rows
