@@ -332,9 +332,17 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         }
       }
       if (fits) {
-        // the local row of every tile nonzero, one byte each (warp w fills rows w, w+12, ...)
-        for (int r = w; r < nrows; r += kBuilders / 32)
-          for (int g = s_rp[r] + lane; g < s_rp[r + 1]; g += 32) s_rowid[g - p0] = uint8_t(r);
+        // the local row of every tile nonzero, one byte each: thread r fills
+        // row r, 4-byte stores for the aligned middle (no word is shared
+        // between rows there), bytes at the ends
+        for (int r = tid; r < nrows; r += kBuilders) {
+          const int e = s_rp[r + 1] - p0;
+          int g = s_rp[r] - p0;
+          for (; g < e && (g & 3); ++g) s_rowid[g] = uint8_t(r);
+          const uint32_t rep4 = uint32_t(r) * 0x01010101u;
+          for (; g + 4 <= e; g += 4) *reinterpret_cast<uint32_t*>(s_rowid + g) = rep4;
+          for (; g < e; ++g) s_rowid[g] = uint8_t(r);
+        }
       }
       builders_sync();
       if (fits) {
