@@ -117,7 +117,7 @@ KERNEL_SOURCES = {
     "window": ["spmm_window.cuh", "spmm_window.cu"],
     "window_tc": ["spmm_tc_window.cuh", "spmm_tc_window.cu"],
     "smalln": ["spmm_rowgroup.cuh", "spmm_rowgroup.cu"],
-    "sddmm": ["spmm_sddmm.cuh", "spmm_sddmm_f32.cu"],
+    "sddmm": ["spmm_sddmm.cuh", "spmm_sddmm_row.cuh", "spmm_sddmm_f32.cu"],
     "fusedmm": ["spmm_balanced.cuh", "spmm_fusedmm_f32.cu", "spmm_sddmm.cuh"],
 }
 COMMON_SOURCES = ["spmm_device.cuh"]

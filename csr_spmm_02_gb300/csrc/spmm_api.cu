@@ -138,6 +138,15 @@ spmm_status sddmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const floa
   L.K = K;
   L.colind = colind;
   L.B = B;
+  // Short, even rows (a row-class plan) and one 128-column tile: a group per
+  // row keeps the C row in registers.
+  const bool row_family = plan->kernel == SPMM_KERNEL_ROW || plan->kernel == SPMM_KERNEL_WINDOW ||
+                          plan->kernel == SPMM_KERNEL_SMALLN || plan->kernel == SPMM_KERNEL_WINDOW_TC;
+  if (row_family && vector_ok && plan->N <= 128) {
+    const int G = std::max(4, pow2_at_least(plan->N / 4));
+    const cudaError_t e = launch_sddmm_row_f32(L, G, Cd, out);
+    return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+  }
   // Rows wider than one 128-column tile: two or four chunks per lane, so the
   // whole dot product comes from batched loads.
   Shape s = choose_shape_balanced(plan->N, false, vector_ok);

@@ -110,6 +110,8 @@ cudaError_t launch_fixup(const Launch& L, int sr = 0);  // sr: semiring code, 0 
 // (add 0 sum, 1 min, 2 max; mul 0 multiply, 1 add).
 cudaError_t launch_semiring_f32(const Launch& L, Shape s, int sr);
 cudaError_t launch_sddmm_f32(const Launch& L, Shape s, const float* Cd, float* out);
+// SDDMM with one group of G lanes (4, 8, 16, 32) per row: 4 fp32 columns per lane, N <= 4G.
+cudaError_t launch_sddmm_row_f32(const Launch& L, int G, const float* Cd, float* out);
 cudaError_t launch_fusedmm_f32(const Launch& L, Shape s, const float* Cd, const float* Bd);
 // Merge-path coordinates of the P+1 range starts (ranges of T items) into part.
 cudaError_t launch_partition(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t T, int32_t P, int2* part,

@@ -1,5 +1,6 @@
-// Instantiations of the SDDMM kernel (fp32).
+// Instantiations of the SDDMM kernels (fp32): merge-path ranges and row groups.
 #include "spmm_sddmm.cuh"
+#include "spmm_sddmm_row.cuh"
 
 namespace spmm {
 
@@ -11,6 +12,16 @@ cudaError_t launch_sddmm_f32(const Launch& L, Shape s, const float* Cd, float* o
   X(4, 32, 2) X(4, 32, 4)  // wide rows
 #undef X
   return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t launch_sddmm_row_f32(const Launch& L, int G, const float* Cd, float* out) {
+  switch (G) {
+    case 4: return launch_sddmm_row_t<4>(L, Cd, out);
+    case 8: return launch_sddmm_row_t<8>(L, Cd, out);
+    case 16: return launch_sddmm_row_t<16>(L, Cd, out);
+    case 32: return launch_sddmm_row_t<32>(L, Cd, out);
+    default: return cudaErrorInvalidConfiguration;
+  }
 }
 
 }  // namespace spmm

@@ -30,9 +30,9 @@ def problem(seed, M=1200, K=800, N=64, integer=False):
     return p, C, B, D
 
 
-def run_sddmm(p, C, B, T=256, arrays=None):
+def run_sddmm(p, C, B, T=256, arrays=None, kernel="auto"):
     a = arrays or H.device_arrays(p)
-    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N, items_per_cta=T)
+    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N, kernel=kernel, items_per_cta=T)
     out = torch.full((p.nnz,), float("nan"), device="cuda")
     spmm.spmm_csr_sddmm_f32(plan, p.K, a["colind"], torch.from_numpy(C).cuda(), torch.from_numpy(B).cuda(), out)
     torch.cuda.synchronize()
@@ -62,6 +62,20 @@ def test_sddmm_parity(N):
     got = run_sddmm(p, C, B)
     ref, S = oracle.sddmm_reference(p.rowptr, p.colind, C, B)
     assert np.all(np.abs(got - ref) <= 1e-5 * S + 1e-30)
+
+
+@pytest.mark.parametrize("N", [4, 8, 12, 16, 20, 32, 60, 64, 100, 128])
+def test_sddmm_row_groups(N):
+    """Row-class plans with N <= 128 take the group-per-row SDDMM (C row in registers): empty rows,
+    rows longer than many rounds, ragged last rounds, lanes past N; integer data is exact."""
+    for integer in (False, True):
+        p, C, B, _ = problem(300 + N, N=N, integer=integer)
+        got = run_sddmm(p, C, B, kernel="row")
+        ref, S = oracle.sddmm_reference(p.rowptr, p.colind, C, B)
+        if integer:
+            assert np.array_equal(got, ref)
+        else:
+            assert np.all(np.abs(got - ref) <= 1e-5 * S + 1e-30)
 
 
 @pytest.mark.parametrize("N", [1, 3, 4, 8, 32, 33, 64, 128, 130, 256, 600])
