@@ -118,7 +118,7 @@ KERNEL_SOURCES = {
     "window_tc": ["spmm_tc_window.cuh", "spmm_tc_window.cu"],
     "smalln": ["spmm_rowgroup.cuh", "spmm_rowgroup.cu"],
     "sddmm": ["spmm_sddmm.cuh", "spmm_sddmm_row.cuh", "spmm_sddmm_f32.cu"],
-    "fusedmm": ["spmm_balanced.cuh", "spmm_fusedmm_f32.cu", "spmm_sddmm.cuh"],
+    "fusedmm": ["spmm_balanced.cuh", "spmm_fusedmm_f32.cu", "spmm_sddmm.cuh", "spmm_sddmm_row.cuh"],
 }
 COMMON_SOURCES = ["spmm_device.cuh"]
 
@@ -411,7 +411,9 @@ def gpu_arm(args, p, cfg, ws, rank, local):
         def step(t=d):
             spmm.spmm_csr_sddmm_f32(plan, p.K, t["colind"], t["C"], t["B"], out)
     else:
-        kernel, launches_per_step = "fusedmm", 2
+        # row-class plans with N <= 128 run the group-per-row FusedMM (no fixup launch)
+        row_form = info["kernel"] in ("row", "window", "smalln", "window_tc") and p.N <= 128
+        kernel, launches_per_step = "fusedmm", 1 if row_form else 2
 
         def step(t=d):
             spmm.spmm_csr_fusedmm_f32(plan, p.K, t["colind"], t["C"], t["B"], t["D"], out)

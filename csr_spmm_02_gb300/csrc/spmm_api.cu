@@ -198,6 +198,15 @@ spmm_status fusedmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const fl
   L.colind = colind;
   L.B = D;  // gathered and accumulated
   L.C = E;
+  // Short, even rows (a row-class plan) and one 128-column tile: a group per
+  // row keeps the C row and the E row in registers.
+  const bool row_family = plan->kernel == SPMM_KERNEL_ROW || plan->kernel == SPMM_KERNEL_WINDOW ||
+                          plan->kernel == SPMM_KERNEL_SMALLN || plan->kernel == SPMM_KERNEL_WINDOW_TC;
+  if (row_family && vector_ok && plan->N <= 128) {
+    cudaError_t e = launch_fusedmm_row_f32(L, std::max(4, pow2_at_least(plan->N / 4)), Cd, B);
+    if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+    return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+  }
   // Every column tile recomputes the dot products over all N columns, so wide
   // rows take one tile of up to 512 columns (two or four chunks per lane).
   Shape s = choose_shape_balanced(plan->N, false, vector_ok);

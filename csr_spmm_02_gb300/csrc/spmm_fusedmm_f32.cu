@@ -1,5 +1,7 @@
-// Instantiations of the balanced kernel in FusedMM mode (fp32).
+// Instantiations of the FusedMM kernels (fp32): the balanced kernel in
+// FusedMM mode and the group-per-row form.
 #include "spmm_balanced.cuh"
+#include "spmm_sddmm_row.cuh"
 
 namespace spmm {
 
@@ -11,6 +13,16 @@ cudaError_t launch_fusedmm_f32(const Launch& L, Shape s, const float* Cd, const 
   X(4, 32, 2) X(4, 32, 4)  // one tile for wide rows
 #undef X
   return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t launch_fusedmm_row_f32(const Launch& L, int G, const float* Cd, const float* Bd) {
+  switch (G) {
+    case 4: return launch_fusedmm_row_t<4>(L, Cd, Bd);
+    case 8: return launch_fusedmm_row_t<8>(L, Cd, Bd);
+    case 16: return launch_fusedmm_row_t<16>(L, Cd, Bd);
+    case 32: return launch_fusedmm_row_t<32>(L, Cd, Bd);
+    default: return cudaErrorInvalidConfiguration;
+  }
 }
 
 }  // namespace spmm

@@ -113,6 +113,8 @@ cudaError_t launch_sddmm_f32(const Launch& L, Shape s, const float* Cd, float* o
 // SDDMM with one group of G lanes (4, 8, 16, 32) per row: 4 fp32 columns per lane, N <= 4G.
 cudaError_t launch_sddmm_row_f32(const Launch& L, int G, const float* Cd, float* out);
 cudaError_t launch_fusedmm_f32(const Launch& L, Shape s, const float* Cd, const float* Bd);
+// FusedMM with one group of G lanes (4, 8, 16, 32) per row: 4 fp32 columns per lane, N <= 4G; L.B is D.
+cudaError_t launch_fusedmm_row_f32(const Launch& L, int G, const float* Cd, const float* Bd);
 // Merge-path coordinates of the P+1 range starts (ranges of T items) into part.
 cudaError_t launch_partition(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t T, int32_t P, int2* part,
                              cudaStream_t stream);

@@ -1,4 +1,5 @@
-// SDDMM for short, even rows: one group of G lanes per row, persistent.
+// SDDMM and FusedMM for short, even rows: one group of G lanes per row,
+// persistent.
 //
 // The SDDMM section of "Performance Optimization of Deep Learning Sparse
 // Matrix Kernels on Intel Max Series GPU" (Algorithm 1, Figs. 3-4) keeps the
@@ -135,6 +136,130 @@ cudaError_t launch_sddmm_row_t(const Launch& L, const float* Cd, float* out) {
   const unsigned grid = unsigned(std::min<int64_t>(need, sddmm_row_blocks<G>(dev)));
   spmm_sddmm_row_kernel<G><<<grid, kThreads, 0, L.stream>>>(L.M, L.N, L.rowptr, L.colind, Cd,
                                                             static_cast<const float*>(L.B), out);
+  return cudaGetLastError();
+}
+
+}  // namespace spmm
+
+namespace spmm {
+
+// FusedMM for short, even rows (the FusedMM section of the same page, Fig. 6,
+// Algorithm 3): E_i = sum_j (C_i . B_j) D_j with one group of G lanes per
+// row, persistent as above.  A round of G nonzeros first gathers their B rows
+// for the dot products (C_i in registers), sums them over the group with the
+// transposed butterfly, then gathers their D rows and accumulates each with
+// its value, handed from lane t by a group shuffle.  E_i stays in registers
+// and is stored once; the values never reach memory.
+template <int G>
+__global__ void __launch_bounds__(kThreads)
+    spmm_fusedmm_row_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr,
+                            const int32_t* __restrict__ colind, const float* __restrict__ Cd,
+                            const float* __restrict__ B, const float* __restrict__ D, float* __restrict__ E) {
+  constexpr int VEC = 4;
+  constexpr int kGroups = kThreads / G;
+  constexpr int U = 4;  // gathers in flight per lane
+  __shared__ int s_c[kGroups * G];
+
+  const int lane = threadIdx.x & (G - 1);
+  const int grp = threadIdx.x / G;
+  const int64_t stride = int64_t(gridDim.x) * kGroups;
+  int64_t row = int64_t(blockIdx.x) * kGroups + grp;
+  if (row >= M) return;
+  const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << ((threadIdx.x & 31) & ~(G - 1)));
+  int* cb = s_c + grp * G;
+
+  const int coff = lane * VEC;
+  const bool valid = coff < N;
+  const int cl = min(coff, N - VEC);
+  const uint64_t stream_pol = policy_evict_first();
+
+  int start = ld_stream(rowptr + row, stream_pol);
+  int end = ld_stream(rowptr + row + 1, stream_pol);
+  int pc = start + lane < end ? ld_stream(colind + start + lane, stream_pol) : 0;
+  for (; row < M; row += stride) {
+    const int64_t nrow = row + stride;
+    int nstart = 0, nend = 0;
+    if (nrow < M) {
+      nstart = ld_stream(rowptr + nrow, stream_pol);
+      nend = ld_stream(rowptr + nrow + 1, stream_pol);
+    }
+    FVec<VEC> c, acc;
+    acc.zero();
+    if (end > start) {
+      BSlice<float, VEC> cs;
+      cs.load(Cd + size_t(row) * N + cl);
+      cs.widen(c);
+    }
+    for (int base = start; base < end; base += G) {
+      const int cnt = min(G, end - base);
+      __syncwarp(gmask);
+      cb[lane] = pc;
+      __syncwarp(gmask);
+      if (base + G < end) pc = base + G + lane < end ? ld_stream(colind + base + G + lane, stream_pol) : 0;
+      else pc = nstart + lane < nend ? ld_stream(colind + nstart + lane, stream_pol) : 0;
+      float d[G];
+#pragma unroll
+      for (int t0 = 0; t0 < G; t0 += U) {  // dot products with the round's B rows
+        BSlice<float, VEC> bs[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) bs[u].load(B + size_t(cb[min(t0 + u, cnt - 1)]) * N + cl);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          FVec<VEC> b;
+          bs[u].widen(b);
+          float2 t = __fmul2_rn(c.p[0], b.p[0]);
+          t = __ffma2_rn(c.p[1], b.p[1], t);
+          d[t0 + u] = valid ? t.x + t.y : 0.f;
+        }
+      }
+      const float x = group_reduce_transposed_masked<G>(d, lane, gmask);  // lane t: value of nonzero t
+#pragma unroll
+      for (int t0 = 0; t0 < G; t0 += U) {  // accumulate the round's D rows
+        if (t0 >= cnt) break;
+        BSlice<float, VEC> ds[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) ds[u].load(D + size_t(cb[min(t0 + u, cnt - 1)]) * N + cl);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float v = __shfl_sync(gmask, x, t0 + u, G);
+          FVec<VEC> dv;
+          ds[u].widen(dv);
+          acc.fma(pair(t0 + u < cnt ? v : 0.f), dv);
+        }
+      }
+    }
+    if (start == end) pc = nstart + lane < nend ? ld_stream(colind + nstart + lane, stream_pol) : 0;
+    if (valid) store_c<VEC>(E + size_t(row) * N + coff, acc);
+    start = nstart;
+    end = nend;
+  }
+}
+
+template <int G>
+int fusedmm_row_blocks(int dev) {
+  static int cached[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  if (!cached[dev]) {
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, spmm_fusedmm_row_kernel<G>, kThreads, 0) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 1;
+    cached[dev] = std::max(1, per_sm) * std::max(1, sms);
+  }
+  return cached[dev];
+}
+
+template <int G>
+cudaError_t launch_fusedmm_row_t(const Launch& L, const float* Cd, const float* Bd) {
+  constexpr int kGroups = kThreads / G;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int64_t need = (int64_t(L.M) + kGroups - 1) / kGroups;
+  const unsigned grid = unsigned(std::min<int64_t>(need, fusedmm_row_blocks<G>(dev)));
+  spmm_fusedmm_row_kernel<G><<<grid, kThreads, 0, L.stream>>>(L.M, L.N, L.rowptr, L.colind, Cd, Bd,
+                                                              static_cast<const float*>(L.B), L.C);
   return cudaGetLastError();
 }
 

@@ -39,9 +39,9 @@ def run_sddmm(p, C, B, T=256, arrays=None, kernel="auto"):
     return out.cpu().numpy().astype(np.float64)
 
 
-def run_fusedmm(p, C, B, D, T=256, arrays=None):
+def run_fusedmm(p, C, B, D, T=256, arrays=None, kernel="auto"):
     a = arrays or H.device_arrays(p)
-    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N, items_per_cta=T)
+    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N, kernel=kernel, items_per_cta=T)
     E = torch.full((p.M, p.N), float("nan"), device="cuda")
     spmm.spmm_csr_fusedmm_f32(plan, p.K, a["colind"], torch.from_numpy(C).cuda(), torch.from_numpy(B).cuda(),
                               torch.from_numpy(D).cuda(), E)
@@ -76,6 +76,19 @@ def test_sddmm_row_groups(N):
             assert np.array_equal(got, ref)
         else:
             assert np.all(np.abs(got - ref) <= 1e-5 * S + 1e-30)
+
+
+@pytest.mark.parametrize("N", [4, 8, 12, 16, 20, 32, 60, 64, 100, 128])
+def test_fusedmm_row_groups(N):
+    """Row-class plans with N <= 128 take the group-per-row FusedMM (C and E rows in registers)."""
+    for integer in (False, True):
+        p, C, B, D = problem(400 + N, N=N, integer=integer)
+        got = run_fusedmm(p, C, B, D, kernel="row")
+        ref, _ = oracle.fusedmm_reference(p.rowptr, p.colind, C, B, D)
+        if integer:
+            assert np.array_equal(got, ref)
+        else:
+            H.assert_within(got, ref, fused_bound(p, C, B, D), "f32", f"fusedmm row N={N}")
 
 
 @pytest.mark.parametrize("N", [1, 3, 4, 8, 32, 33, 64, 128, 130, 256, 600])
