@@ -104,7 +104,10 @@ __global__ void __launch_bounds__(kThreads)
         }
       }
       const float x = group_reduce_transposed_masked<G>(d, lane, gmask);
-      if (lane < cnt) st_stream1(out + base + lane, x);
+      // plain store: a group writes 64 bytes of a 128-byte line per round, and
+      // both halves must meet in L2 (an evict-first store let half-written
+      // lines reach DRAM, about 17x the output's bytes)
+      if (lane < cnt) out[base + lane] = x;
     }
     if (start == end) pc = nstart + lane < nend ? ld_stream(colind + nstart + lane, stream_pol) : 0;
     start = nstart;
