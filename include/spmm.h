@@ -157,8 +157,8 @@ SPMM_API spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t 
 SPMM_API spmm_status spmm_plan_set_group_lanes(spmm_plan_t plan, int32_t lanes);
 
 /*
- * N-slicing (survey of L2-level chunking; the kkmem page's chunking moved from
- * host/HBM to L2/HBM): cap the column tile of the row and balanced kernels at
+ * N-slicing (L2-level chunking: the kkmem page's multilevel chunking moved
+ * from host/HBM to L2/HBM): cap the column tile of the row and balanced kernels at
  * `columns` (0 removes the cap), so that each tile's slice of B (K x tile
  * columns) is what L2 holds at a time; the tiles run in order.  The plan's
  * own choice is one tile: on the measured workloads narrower tiles were
