@@ -58,6 +58,9 @@
 #ifndef SPMM_BAL_MIN_BLOCKS
 #define SPMM_BAL_MIN_BLOCKS 4  // resident CTAs asked of the compiler (fp32, one chunk per lane)
 #endif
+#ifndef SPMM_FUSED_MIN_BLOCKS
+#define SPMM_FUSED_MIN_BLOCKS 3  // the same for FusedMM (80 registers)
+#endif
 
 namespace spmm {
 
@@ -73,10 +76,12 @@ struct BalancedSteps {
 
 // The 64-register budget of 4 resident CTAs fits the fp32 one-chunk SpMM
 // shapes without spills; FusedMM (two gathered operands per nonzero plus the
-// C slices) gets 128 registers; wider or bf16 lanes keep the compiler's choice.
+// C slices) gets 80 (3 CTAs: more gathers in flight per SM than 2 CTAs of 128
+// registers, without the spills of 4); wider or bf16 lanes keep the
+// compiler's choice.
 template <typename BT, int NCH, bool FUSED>
 struct BalancedMinBlocks {
-  static constexpr int value = FUSED ? 2 : (sizeof(BT) == 4 && NCH == 1) ? SPMM_BAL_MIN_BLOCKS : 1;
+  static constexpr int value = FUSED ? SPMM_FUSED_MIN_BLOCKS : (sizeof(BT) == 4 && NCH == 1) ? SPMM_BAL_MIN_BLOCKS : 1;
 };
 
 __host__ __device__ constexpr size_t balanced_smem_layout_bytes(int W, int TW, int T) {

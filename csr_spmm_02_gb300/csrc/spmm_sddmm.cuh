@@ -35,6 +35,9 @@
 #ifndef SPMM_SDDMM_LOADS_WIDE
 #define SPMM_SDDMM_LOADS_WIDE 2  // the same for 32-lane groups (each lane already keeps 32 partial sums)
 #endif
+#ifndef SPMM_SDDMM_MIN_BLOCKS
+#define SPMM_SDDMM_MIN_BLOCKS 4  // resident CTAs asked of the compiler (64 registers; a few spill)
+#endif
 
 namespace spmm {
 
@@ -43,16 +46,32 @@ __host__ __device__ constexpr size_t sddmm_smem_layout_bytes(int T) {
 }
 
 // Local row of every staged nonzero n in [p0, p1): the largest r <= last_row
-// with rp[r] <= n (rows with no nonzeros are skipped by that rule).  Ends with
-// a CTA barrier.
+// with rp[r] <= n (rows with no nonzeros are skipped by that rule).  Each
+// thread takes one run of consecutive nonzeros (an odd run length, so the
+// threads' runs start in distinct banks), finds the row of its first one by
+// binary search and walks the row ends from there.  Ends with a CTA barrier.
 __device__ __forceinline__ void fill_row_ids(const int* rp, int last_row, int p0, int p1, int nbase, int* s_row) {
-  for (int n = p0 + int(threadIdx.x); n < p1; n += kThreads) {
+  const int count = p1 - p0;
+  int per = (count + kThreads - 1) / kThreads;
+  if (per > 0 && (per & 1) == 0) ++per;
+  const int k0 = min(int(threadIdx.x) * per, count), k1 = min(k0 + per, count);
+  if (k0 < k1) {
+    const int n0 = p0 + k0;
     int lo = 0, hi = last_row;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (rp[mid] <= n) lo = mid; else hi = mid - 1;
+      if (rp[mid] <= n0) lo = mid; else hi = mid - 1;
     }
-    s_row[n - nbase] = lo;
+    int r = lo;
+    int next = r < last_row ? rp[r + 1] : INT_MAX;  // first nonzero after row r
+#pragma unroll 1
+    for (int n = n0; n < p0 + k1; ++n) {
+      while (n >= next) {  // row r ended (empty rows end at once)
+        ++r;
+        next = r < last_row ? rp[r + 1] : INT_MAX;
+      }
+      s_row[n - nbase] = r;
+    }
   }
   __syncthreads();
 }
@@ -131,7 +150,7 @@ __device__ __forceinline__ float group_reduce_transposed(float (&v)[P], int gl) 
 }
 
 template <int VEC, int G, int NCH>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, SPMM_SDDMM_MIN_BLOCKS)
     spmm_sddmm_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr, const int32_t* __restrict__ colind,
                       const float* __restrict__ Cd, const float* __restrict__ B, float* __restrict__ out,
                       const int2* __restrict__ part, int32_t T, int* __restrict__ err) {
