@@ -75,13 +75,16 @@ struct BalancedSteps {
 };
 
 // The 64-register budget of 4 resident CTAs fits the fp32 one-chunk SpMM
-// shapes without spills; FusedMM (two gathered operands per nonzero plus the
-// C slices) gets 80 (3 CTAs: more gathers in flight per SM than 2 CTAs of 128
-// registers, without the spills of 4); wider or bf16 lanes keep the
-// compiler's choice.
-template <typename BT, int NCH, bool FUSED>
+// shapes without spills; wider or bf16 lanes keep the compiler's choice.
+// FusedMM (two gathered operands per nonzero plus the C slices) runs 3 CTAs
+// of 80 registers where its one-chunk, multi-lane shapes fit them (more
+// gathers in flight per SM than 2 CTAs of 128 registers, without the spills
+// of 4); the shapes that would spill more (one lane per nonzero, two or more
+// chunks per lane) keep 2.
+template <typename BT, int G, int NCH, bool FUSED>
 struct BalancedMinBlocks {
-  static constexpr int value = FUSED ? SPMM_FUSED_MIN_BLOCKS : (sizeof(BT) == 4 && NCH == 1) ? SPMM_BAL_MIN_BLOCKS : 1;
+  static constexpr int fused = (NCH == 1 && G >= 2) ? SPMM_FUSED_MIN_BLOCKS : 2;
+  static constexpr int value = FUSED ? fused : (sizeof(BT) == 4 && NCH == 1) ? SPMM_BAL_MIN_BLOCKS : 1;
 };
 
 __host__ __device__ constexpr size_t balanced_smem_layout_bytes(int W, int TW, int T) {
@@ -92,7 +95,7 @@ __host__ __device__ constexpr size_t balanced_smem_layout_bytes(int W, int TW, i
 }
 
 template <typename BT, int VEC, int G, int NCH, bool FUSED, int SR>
-__global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, NCH, FUSED>::value)
+__global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>::value)
     spmm_balanced_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr,
                          const int32_t* __restrict__ colind, const float* __restrict__ vals,
                          const BT* __restrict__ B, float* __restrict__ C,
