@@ -18,7 +18,8 @@
 //     coalesced row caching the Sgap page cites from Ge-SpMM), plain loads for
 //     the unaligned ends;
 //  2. cuts the range again into one sub-range per warp with the same search
-//     in shared memory.  A warp is one worker: its 32 lanes form S = 32/G
+//     in shared memory, a row end weighing as much as the nonzeros of two
+//     warp steps (the work it costs a warp).  A warp is one worker: its 32 lanes form S = 32/G
 //     groups of G lanes, each lane owning NCH 16-byte chunks of the output
 //     row; a step gives S consecutive nonzeros to the S groups (Sgap's
 //     {<1 nnz, c col>, r = S} point), so every branch is uniform in the warp;
@@ -57,6 +58,9 @@
 #endif
 #ifndef SPMM_BAL_MIN_BLOCKS
 #define SPMM_BAL_MIN_BLOCKS 4  // resident CTAs asked of the compiler (fp32, one chunk per lane)
+#endif
+#ifndef SPMM_BAL_ROW_WEIGHT
+#define SPMM_BAL_ROW_WEIGHT 0  // items a row end counts for in the warps' split (0: by shape, below)
 #endif
 #ifndef SPMM_FUSED_MIN_BLOCKS
 #define SPMM_FUSED_MIN_BLOCKS 3  // the same for FusedMM (80 registers)
@@ -183,20 +187,31 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>
   const int* rp = s_rp + (i0 - rbase);  // rp[r] = rowptr[i0 + r], 0 <= r <= i1 - i0
   int* const s_row = reinterpret_cast<int*>(s_val);
   if constexpr (FUSED) fill_row_ids(rp, i1 - i0, p0, p1, nbase, s_row);
-  const int items = (i1 - i0) + (p1 - p0);
-  const int Tw = T / W;
-  auto find_row = [&](int dl) {  // first local row whose end lies at or after diagonal dl
+  // The warps split the range's merged sequence with each row end counted as
+  // kRowWeight items: row r's end sits at cost E(r) = (rowptr[r+1] - p0) +
+  // kRowWeight * r, and a warp starting at cost c begins at the first row with
+  // E(r) >= c and at the nonzeros of that row whose cost lies below c.  A row
+  // end costs a warp about two steps (its butterfly and store) and a step
+  // takes S nonzeros, so a row end weighs 2S nonzeros (capped at 16; measured
+  // best on rmat22 at S = 4 and rmat20 at S = 1).  FusedMM spends far more on
+  // each nonzero and keeps the plain merge path (weight 1).
+  constexpr int kRowWeight = SPMM_BAL_ROW_WEIGHT > 0 ? SPMM_BAL_ROW_WEIGHT : FUSED ? 1 : (2 * S < 16 ? 2 * S : 16);
+  const int cost = (p1 - p0) + kRowWeight * (i1 - i0);
+  auto find_row = [&](int c) {  // first local row whose end costs c or more
     int lo = 0, hi = i1 - i0;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (rp[mid + 1] - p0 + mid >= dl) hi = mid; else lo = mid + 1;
+      if (rp[mid + 1] - p0 + kRowWeight * mid >= c) hi = mid; else lo = mid + 1;
     }
     return lo;
   };
-  const int dl0 = min(w * Tw, items);
-  const int dl1 = min(dl0 + Tw, items);
-  const int rw0 = find_row(dl0), rw1 = find_row(dl1);
-  const int pw0 = p0 + dl0 - rw0, pw1 = p0 + dl1 - rw1;
+  auto nz_start = [&](int c, int r) {  // first nonzero of the warp starting at cost c in row r
+    const int hi = r < i1 - i0 ? rp[r + 1] : p1;
+    return p0 + min(max(c - kRowWeight * r, rp[r] - p0), hi - p0);
+  };
+  const int c0 = int((int64_t(cost) * w) / W), c1 = int((int64_t(cost) * (w + 1)) / W);
+  const int rw0 = find_row(c0), rw1 = find_row(c1);
+  const int pw0 = nz_start(c0, rw0), pw1 = nz_start(c1, rw1);
 
   const int col0 = blockIdx.y * TW;
   int coff[NCH];
