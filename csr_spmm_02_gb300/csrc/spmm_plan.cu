@@ -252,7 +252,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   // merge-path partition and carry rows: used by the balanced SpMM, SDDMM and
   // FusedMM (a one-call SpMM on another kernel needs neither)
   if (!one_call || plan->kernel == SPMM_KERNEL_BALANCED) {
-    const int T = items_per_cta ? items_per_cta : kDefaultItemsPerCta;
+    const int T = items_per_cta ? items_per_cta : default_items_per_cta(N);
     const int64_t total = int64_t(M) + nnz;
     const int64_t P = (total + T - 1) / T;
     if (P > INT32_MAX - 1) return fail(SPMM_ERR_UNSUPPORTED);

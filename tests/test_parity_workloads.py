@@ -15,7 +15,7 @@ from tests import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
 
-DEFAULT_T = 2048
+PLAN_TS = (2048, 3072)  # the plan's default range sizes (N > 32, N <= 32)
 
 
 def boundary_rows(rowptr, T, limit=3000):
@@ -34,7 +34,7 @@ def sample_rows(p, rng):
     lens = np.diff(p.rowptr)
     longest = np.argsort(lens)[-64:]
     rand = rng.choice(p.M, 6000, replace=False)
-    return np.unique(np.concatenate([longest, rand, boundary_rows(p.rowptr, DEFAULT_T), [0, p.M - 1]])).astype(np.int32)
+    return np.unique(np.concatenate([longest, rand, *[boundary_rows(p.rowptr, T) for T in PLAN_TS], [0, p.M - 1]])).astype(np.int32)
 
 
 @pytest.mark.parametrize("name", gen.WORKLOAD_ORDER)
