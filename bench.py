@@ -210,6 +210,19 @@ def op_bytes(p, op):
     return pattern + dense + 4 * p.K * p.N + 4 * p.M * p.N  # + D, E
 
 
+def op_gather_bytes(p, op, kernel):
+    """Bytes of B rows (and D rows for FusedMM) that a gathering kernel reads
+    per launch: one N-wide row slice per nonzero and operand.  They come
+    through L2 whether or not they stay there, so this stream rather than
+    HBM bounds the gather kernels when B fits L2.  None for the window
+    kernels, which stage each window of B rows once."""
+    if kernel in ("window", "window_tc"):
+        return None
+    if op == "spmm":
+        return p.nnz * p.N * (2 if p.b_dtype == "bf16" else 4)
+    return (1 if op == "sddmm" else 2) * p.nnz * p.N * 4
+
+
 def op_dense_inputs(p, op):
     """fp32 operands of SDDMM / FusedMM on the workload's pattern: (C, B, D).
 
@@ -480,6 +493,10 @@ def gpu_arm(args, p, cfg, ws, rank, local):
     mean_main = sum(main_ms) / len(main_ms)
     achieved = nbytes / (mean_main * 1e-3) / 1e9
     traffic = ncu_traffic(p.name if op == "spmm" else f"{p.name}:{op}", kernel)
+    gbytes = op_gather_bytes(p, op, kernel)
+    gather = None if gbytes is None else {
+        "bytes_per_launch": gbytes, "achieved_tbs": gbytes / (mean_main * 1e-3) / 1e12, "unit": "TB/s",
+        "what": "B rows gathered per nonzero (nnz x N x sizeof(B); B and D for FusedMM), read through L2"}
     eff_gbs = nbytes / (ms_per_step * 1e-3) / 1e9
 
     # end to end: pinned host inputs -> device, the public call, result -> pinned host
@@ -556,6 +573,7 @@ def gpu_arm(args, p, cfg, ws, rank, local):
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes": nbytes, "kernel_ms": mean_main},
+        "gather": gather,
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_par, "e2e": e2e, "clocks": clocks,
         "gpu_launches": steps * launches_per_step,
     }

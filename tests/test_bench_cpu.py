@@ -20,6 +20,14 @@ def test_op_bytes_and_flops():
     assert bench.op_flops(p, "fusedmm") == 4 * nnz * N
 
 
+def test_gather_bytes():
+    p = gen.make_workload("uniform1k")  # fp32 B, N = 32
+    assert bench.op_gather_bytes(p, "spmm", "row") == p.nnz * p.N * 4
+    assert bench.op_gather_bytes(p, "sddmm", "balanced") == p.nnz * p.N * 4
+    assert bench.op_gather_bytes(p, "fusedmm", "fusedmm") == 2 * p.nnz * p.N * 4
+    assert bench.op_gather_bytes(p, "spmm", "window_tc") is None
+
+
 def test_dense_operands_are_seeded_fp32():
     p = gen.make_workload("uniform1k")
     C1, B1, D1 = bench.op_dense_inputs(p, "fusedmm")
