@@ -128,6 +128,14 @@ def _ptr(t, dtype, name, allow_none=False):
     return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
 
 
+def _need(t, n, name):
+    """Refuse a buffer smaller than the call will read or write (checked before
+    any pointer reaches the library, so a short buffer never becomes an
+    out-of-bounds access on the device)."""
+    if t is not None and t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements; the call needs at least {n}")
+
+
 _I32 = (torch.int32,)
 _F32 = (torch.float32,)
 _BF16_BITS = (torch.uint16, torch.int16, torch.bfloat16) if hasattr(torch, "uint16") else (torch.int16, torch.bfloat16)
@@ -136,9 +144,10 @@ _BF16_BITS = (torch.uint16, torch.int16, torch.bfloat16) if hasattr(torch, "uint
 class Plan:
     """Owns a ``spmm_plan_t``; keeps the rowptr tensor alive while the plan lives."""
 
-    def __init__(self, handle: int, rowptr: torch.Tensor):
+    def __init__(self, handle: int, rowptr: torch.Tensor, M: int = 0, nnz: int = 0, N: int = 0):
         self.handle = ctypes.c_void_p(handle)
         self.rowptr = rowptr
+        self.M, self.nnz, self.N = M, nnz, N  # the sizes the plan is bound to
 
     def info(self) -> dict:
         pi = PlanInfo()
@@ -160,14 +169,23 @@ class Plan:
 
 
 def spmm_csr_plan(rowptr, M, nnz, N, kernel="auto", items_per_cta=0, stream=None) -> Plan:
+    _need(rowptr, M + 1, "rowptr")
     out = ctypes.c_void_p()
     st = load().spmm_csr_plan_ex(_ptr(rowptr, _I32, "rowptr"), M, nnz, N, KERNELS[kernel], items_per_cta,
                                  _stream(stream), ctypes.byref(out))
     _check(st, "spmm_csr_plan")
-    return Plan(out.value, rowptr)
+    return Plan(out.value, rowptr, M, nnz, N)
+
+
+def _need_exec(plan, K, colind, vals, B, C):
+    _need(colind, plan.nnz, "colind")
+    _need(vals, plan.nnz, "vals")
+    _need(B, K * plan.N, "B")
+    _need(C, plan.M * plan.N, "C")
 
 
 def spmm_csr_f32_exec(plan: Plan, K, colind, vals, B, C, stream=None):
+    _need_exec(plan, K, colind, vals, B, C)
     _check(load().spmm_csr_f32_exec(plan.handle, K, _ptr(colind, _I32, "colind", True),
                                     _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True),
                                     _ptr(C, _F32, "C"), _stream(stream)), "spmm_csr_f32_exec")
@@ -175,13 +193,21 @@ def spmm_csr_f32_exec(plan: Plan, K, colind, vals, B, C, stream=None):
 
 
 def spmm_csr_bf16f32_exec(plan: Plan, K, colind, vals, B, C, stream=None):
+    _need_exec(plan, K, colind, vals, B, C)
     _check(load().spmm_csr_bf16f32_exec(plan.handle, K, _ptr(colind, _I32, "colind", True),
                                         _ptr(vals, _F32, "vals", True), _ptr(B, _BF16_BITS, "B", True),
                                         _ptr(C, _F32, "C"), _stream(stream)), "spmm_csr_bf16f32_exec")
     return C
 
 
+def _need_one_call(M, K, N, rowptr, B, C):
+    _need(rowptr, M + 1, "rowptr")  # nnz = rowptr[M] is only known on the device
+    _need(B, K * N, "B")
+    _need(C, M * N, "C")
+
+
 def spmm_csr_f32(M, K, N, rowptr, colind, vals, B, C, stream=None):
+    _need_one_call(M, K, N, rowptr, B, C)
     _check(load().spmm_csr_f32(M, K, N, _ptr(rowptr, _I32, "rowptr"), _ptr(colind, _I32, "colind", True),
                                _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True), _ptr(C, _F32, "C"),
                                _stream(stream)), "spmm_csr_f32")
@@ -189,6 +215,7 @@ def spmm_csr_f32(M, K, N, rowptr, colind, vals, B, C, stream=None):
 
 
 def spmm_csr_bf16f32(M, K, N, rowptr, colind, vals, B, C, stream=None):
+    _need_one_call(M, K, N, rowptr, B, C)
     _check(load().spmm_csr_bf16f32(M, K, N, _ptr(rowptr, _I32, "rowptr"), _ptr(colind, _I32, "colind", True),
                                    _ptr(vals, _F32, "vals", True), _ptr(B, _BF16_BITS, "B", True),
                                    _ptr(C, _F32, "C"), _stream(stream)), "spmm_csr_bf16f32")
@@ -197,6 +224,10 @@ def spmm_csr_bf16f32(M, K, N, rowptr, colind, vals, B, C, stream=None):
 
 def spmm_csr_sddmm_f32(plan: Plan, K, colind, C, B, out, stream=None):
     """out[p] = C[i] . B[colind[p]] on A's pattern (fp32)."""
+    _need(colind, plan.nnz, "colind")
+    _need(C, plan.M * plan.N, "C")
+    _need(B, K * plan.N, "B")
+    _need(out, plan.nnz, "out")
     _check(load().spmm_csr_sddmm_f32(plan.handle, K, _ptr(colind, _I32, "colind", True), _ptr(C, _F32, "C", True),
                                      _ptr(B, _F32, "B", True), _ptr(out, _F32, "out", True), _stream(stream)),
            "spmm_csr_sddmm_f32")
@@ -222,6 +253,7 @@ def spmm_csr_semiring_f32_exec(plan: Plan, K, colind, vals, B, C, add="sum", mul
 
     add in {"sum", "min", "max"}, mul in {"mul", "add"}; an empty row gives the
     identity of add (0, +inf, -inf)."""
+    _need_exec(plan, K, colind, vals, B, C)
     _check(load().spmm_csr_semiring_f32_exec(plan.handle, K, _ptr(colind, _I32, "colind", True),
                                              _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True),
                                              _ptr(C, _F32, "C"), ADD_OPS[add], MUL_OPS[mul], _stream(stream)),
@@ -231,6 +263,11 @@ def spmm_csr_semiring_f32_exec(plan: Plan, K, colind, vals, B, C, add="sum", mul
 
 def spmm_csr_fusedmm_f32(plan: Plan, K, colind, C, B, D, E, stream=None):
     """E = SDDMM(C, B on A's pattern) . D without storing the SDDMM values (fp32)."""
+    _need(colind, plan.nnz, "colind")
+    _need(C, plan.M * plan.N, "C")
+    _need(B, K * plan.N, "B")
+    _need(D, K * plan.N, "D")
+    _need(E, plan.M * plan.N, "E")
     _check(load().spmm_csr_fusedmm_f32(plan.handle, K, _ptr(colind, _I32, "colind", True), _ptr(C, _F32, "C", True),
                                        _ptr(B, _F32, "B", True), _ptr(D, _F32, "D", True), _ptr(E, _F32, "E"),
                                        _stream(stream)), "spmm_csr_fusedmm_f32")
@@ -239,6 +276,9 @@ def spmm_csr_fusedmm_f32(plan: Plan, K, colind, C, B, D, E, stream=None):
 
 def spmm_csr_f32_noalloc(M, K, N, nnz, rowptr, colind, vals, B, C, stream=None):
     """C = A . B (fp32) with the library's fixed scratch array: no allocation anywhere."""
+    _need_one_call(M, K, N, rowptr, B, C)
+    _need(colind, nnz, "colind")
+    _need(vals, nnz, "vals")
     _check(load().spmm_csr_f32_noalloc(M, K, N, nnz, _ptr(rowptr, _I32, "rowptr"), _ptr(colind, _I32, "colind", True),
                                        _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True), _ptr(C, _F32, "C"),
                                        _stream(stream)), "spmm_csr_f32_noalloc")

@@ -70,6 +70,35 @@ def test_binding_refuses_cpu_tensors(lib):
         spmm.spmm_csr_plan(torch.zeros(5, dtype=torch.int32), 4, 0, 8)
 
 
+def test_binding_refuses_short_buffers(lib):
+    """Buffer sizes are checked against the plan (or the call's sizes) before
+    any pointer reaches the library."""
+    import torch
+    f32 = lambda n: torch.zeros(n, dtype=torch.float32)  # noqa: E731
+    i32 = lambda n: torch.zeros(n, dtype=torch.int32)  # noqa: E731
+    plan = spmm.Plan(0, i32(5), M=4, nnz=6, N=8)  # M=4, nnz=6, N=8; K=3 below
+    cases = [
+        (lambda: spmm.spmm_csr_f32_exec(plan, 3, i32(5), f32(6), f32(24), f32(32)), "colind"),
+        (lambda: spmm.spmm_csr_f32_exec(plan, 3, i32(6), f32(5), f32(24), f32(32)), "vals"),
+        (lambda: spmm.spmm_csr_f32_exec(plan, 3, i32(6), f32(6), f32(23), f32(32)), "B"),
+        (lambda: spmm.spmm_csr_bf16f32_exec(plan, 3, i32(6), f32(6), torch.zeros(24, dtype=torch.int16), f32(31)),
+         "C"),
+        (lambda: spmm.spmm_csr_semiring_f32_exec(plan, 3, i32(6), f32(6), f32(24), f32(31), "min", "add"), "C"),
+        (lambda: spmm.spmm_csr_sddmm_f32(plan, 3, i32(6), f32(32), f32(24), f32(5)), "out"),
+        (lambda: spmm.spmm_csr_fusedmm_f32(plan, 3, i32(6), f32(32), f32(24), f32(23), f32(32)), "D"),
+        (lambda: spmm.spmm_csr_fusedmm_f32(plan, 3, i32(6), f32(32), f32(24), f32(24), f32(31)), "E"),
+        (lambda: spmm.spmm_csr_plan(i32(4), 4, 0, 8), "rowptr"),
+        (lambda: spmm.spmm_csr_f32(4, 3, 8, i32(5), i32(6), f32(6), f32(24), f32(31)), "C"),
+        (lambda: spmm.spmm_csr_f32_noalloc(4, 3, 8, 6, i32(5), i32(6), f32(5), f32(24), f32(32)), "vals"),
+    ]
+    for call, name in cases:
+        with pytest.raises(ValueError, match=f"^{name} holds"):
+            call()
+    # sizes that fit: refused only because the tensors are not on a GPU
+    with pytest.raises(ValueError, match="CUDA"):
+        spmm.spmm_csr_f32_exec(plan, 3, i32(6), f32(6), f32(24), f32(32))
+
+
 C_USER = r"""
 #include <stdio.h>
 #include <stddef.h>
