@@ -231,6 +231,12 @@ spmm_status one_call(int32_t M, int32_t K, int32_t N, const int32_t* rowptr, con
   spmm_plan_t plan = nullptr;
   spmm_status st = spmm_make_plan(rowptr, M, -1, N, SPMM_KERNEL_AUTO, 0, s, true, &plan);
   if (st != SPMM_OK) return st;
+  // The kernels report to the one-call forms' shared error word, which
+  // outlives this plan (spmm_check_device reads it).
+  if (plan->err && call_error_word(&plan->err) != cudaSuccess) {
+    spmm_free_plan(plan, s);
+    return SPMM_ERR_CUDA;
+  }
   st = exec(plan, K, colind, vals, B, bf16, C, s);
   spmm_free_plan(plan, s);
   return st;

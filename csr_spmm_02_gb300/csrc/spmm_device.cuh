@@ -310,6 +310,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // Device error word bits.
-constexpr int kErrStageTimeout = 1;
+constexpr int kErrStageTimeout = 1;  // a bounded wait gave up
+constexpr int kErrInvalidCsr = 2;    // rowptr[M] differs from the nnz the caller passed
 
 }  // namespace spmm

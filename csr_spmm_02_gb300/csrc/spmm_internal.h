@@ -46,8 +46,9 @@ struct spmm_plan_s {
   int64_t workspace_bytes = 0;
   int2* part = nullptr;   // [num_ctas + 1] merge-path coordinates (row, nnz)
   float* carry = nullptr; // [num_ctas][2][N] partial rows split across CTAs
-  int* err = nullptr;     // device error word
-  int* stats = nullptr;   // [2]: max row length, empty rows
+  int* err = nullptr;     // device error word (the plan's own, or the one-call forms' shared word)
+  int* stats = nullptr;   // [3]: max row length, empty rows, rowptr[M]
+  void* small = nullptr;  // the 16-byte allocation holding the plan's own error word and stats
   cudaEvent_t split_event = nullptr;  // recorded between main kernel and fixup
 };
 
@@ -116,8 +117,16 @@ cudaError_t launch_fusedmm_f32(const Launch& L, Shape s, const float* Cd, const 
 // FusedMM with one group of G lanes (4, 8, 16, 32) per row: 4 fp32 columns per lane, N <= 4G; L.B is D.
 cudaError_t launch_fusedmm_row_f32(const Launch& L, int G, const float* Cd, const float* Bd);
 // Merge-path coordinates of the P+1 range starts (ranges of T items) into part.
+// With err: rowptr[M] is compared with nnz on the device; on a mismatch every
+// range is made empty (nothing is read past either array) and kErrInvalidCsr
+// is set in *err.
 cudaError_t launch_partition(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t T, int32_t P, int2* part,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int* err = nullptr);
+
+// Device address of the error word that the one-call forms share on the
+// current device (looked up on every call, so it stays valid after the
+// device's context is reset).
+cudaError_t call_error_word(int** out);
 
 
 constexpr int kDefaultItemsPerCta = 2048;

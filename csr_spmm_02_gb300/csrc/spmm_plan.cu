@@ -33,12 +33,20 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(const int32_t* __re
 
 // part[c] = (row, nonzero) where the merged sequence of nonzeros and row ends
 // is cut at diagonal d = min(c * T, M + nnz): the row is the number of rows
-// whose end position rowptr[r+1] + r lies before d.
+// whose end position rowptr[r+1] + r lies before d.  With err, a caller's nnz
+// that differs from rowptr[M] empties every range (part[c] = (0, 0)) and sets
+// kErrInvalidCsr, so no kernel reads past the nonzeros that exist.
 __global__ void __launch_bounds__(kThreads) merge_path_partition_kernel(const int32_t* __restrict__ rowptr,
                                                                         int32_t M, int64_t nnz, int64_t T,
-                                                                        int32_t P, int2* __restrict__ part) {
+                                                                        int32_t P, int2* __restrict__ part,
+                                                                        int* __restrict__ err) {
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c > P) return;
+  if (err != nullptr && int64_t(__ldg(rowptr + M)) != nnz) {
+    part[c] = make_int2(0, 0);
+    if (c == 0) atomicOr(err, kErrInvalidCsr);
+    return;
+  }
   const int64_t d = min(int64_t(c) * T, int64_t(M) + nnz);
   int lo = 0, hi = M;
   while (lo < hi) {
@@ -109,9 +117,9 @@ cudaError_t launch_fixup(const Launch& L, int sr) {
 }
 
 cudaError_t launch_partition(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t T, int32_t P, int2* part,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, int* err) {
   const unsigned grid = unsigned((int64_t(P) + 1 + kThreads - 1) / kThreads);
-  merge_path_partition_kernel<<<grid, kThreads, 0, stream>>>(rowptr, M, nnz, T, P, part);
+  merge_path_partition_kernel<<<grid, kThreads, 0, stream>>>(rowptr, M, nnz, T, P, part, err);
   return cudaGetLastError();
 }
 
@@ -204,18 +212,17 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
 
   auto fail = [&](spmm_status st) {
     dev_free(plan->workspace, one_call, stream);
-    dev_free(plan->err, one_call, stream);
+    dev_free(plan->small, one_call, stream);
     delete plan;
     return st;
   };
 
   // error word + statistics (16 bytes)
-  void* small = nullptr;
-  cudaError_t e = dev_alloc(&small, 16, one_call, stream);
+  cudaError_t e = dev_alloc(&plan->small, 16, one_call, stream);
   if (e != cudaSuccess) return fail(SPMM_ERR_CUDA);
-  plan->err = static_cast<int*>(small);
+  plan->err = static_cast<int*>(plan->small);
   plan->stats = plan->err + 1;
-  if ((e = cudaMemsetAsync(small, 0, 16, stream)) != cudaSuccess) return fail(SPMM_ERR_CUDA);
+  if ((e = cudaMemsetAsync(plan->small, 0, 16, stream)) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   row_stats_kernel<<<stats_grid(M), kThreads, 0, stream>>>(rowptr, M, plan->stats);
   if ((e = cudaGetLastError()) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   int host_stats[3] = {0, 0, 0};
@@ -267,7 +274,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
     plan->part = static_cast<int2*>(plan->workspace);
     plan->carry = reinterpret_cast<float*>(static_cast<char*>(plan->workspace) + part_padded);
     const unsigned grid = unsigned((P + 1 + kThreads - 1) / kThreads);
-    merge_path_partition_kernel<<<grid, kThreads, 0, stream>>>(rowptr, M, nnz, T, int32_t(P), plan->part);
+    merge_path_partition_kernel<<<grid, kThreads, 0, stream>>>(rowptr, M, nnz, T, int32_t(P), plan->part, nullptr);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   }
   plan->workspace_bytes += 16;
@@ -278,7 +285,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
 void spmm_free_plan(spmm_plan_t plan, cudaStream_t stream) {
   if (!plan) return;
   dev_free(plan->workspace, plan->stream_ordered, stream);
-  dev_free(plan->err, plan->stream_ordered, stream);
+  dev_free(plan->small, plan->stream_ordered, stream);
   delete plan;
 }
 

@@ -43,9 +43,10 @@
 // kErrStageTimeout in the plan's error word and stops instead of hanging.
 //
 // A tile whose column span exceeds three chunks, one holding more than 8448
-// nonzeros, or one with a duplicate (row, column) entry (both nonzero) is
-// computed by the builders with per-row gathers (columns need not be
-// sorted); a tile with
+// nonzeros, one with a duplicate (row, column) entry (both nonzero), or one
+// holding a nonzero value below 2^-110 in magnitude (which the three-term
+// split cannot carry exactly) is computed by the builders with per-row
+// gathers (columns need not be sorted); a tile with
 // no nonzeros stores zero rows.  The dense product multiplies absent entries
 // as zeros, so a NaN/Inf in a B row inside the window reaches every row of
 // the tile; IEEE special values are outside the accepted inputs.
@@ -406,7 +407,11 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
         // every held nonzero into its chunk: value -> three bf16 terms.  A
         // zero value adds nothing and is left out; the hi term of any other
         // value is nonzero, so an atomicOr that finds its half-word already
-        // set has met a second nonzero for the same (row, column).
+        // set has met a second nonzero for the same (row, column).  The split
+        // is exact only for |v| >= 2^-110 (below that the lo term is subnormal
+        // in bf16 and keeps fewer bits; under about 2^-134 even the hi term
+        // rounds to zero): a tile holding a nonzero value of smaller
+        // magnitude is gathered instead, like one with a duplicate.
         bool dup = false;
 #pragma unroll
         for (int i = 0; i < kPerThread; ++i) {
@@ -414,6 +419,7 @@ __global__ void __launch_bounds__(tc::kCtaThreads, 1)
             const int k = int(pk[i] & 0xFFFFu), r = int(pk[i] >> 16);
             const int ch = k >> 6, kk = k & (kChunk - 1);
             const float v = val[i];
+            dup |= v != 0.f && fabsf(v) < 0x1p-110f;
             const uint16_t h = bf16_rn_bits(v);
             if (h != 0) {
               const float r1 = v - bf16_bits_to_float(h);

@@ -39,7 +39,7 @@ EXPORTS = ["spmm_csr_plan", "spmm_csr_plan_ex", "spmm_plan_get_info", "spmm_plan
            "spmm_csr_validate", "spmm_plan_check_device", "spmm_plan_set_split_event",
            "spmm_csr_f32_noalloc", "spmm_csr_sddmm_f32", "spmm_csr_fusedmm_f32", "spmm_csr_semiring_f32_exec",
            "spmm_plan_set_group_lanes", "spmm_plan_set_column_tile", "spmm_pool_release",
-           "spmm_status_string"]
+           "spmm_check_device", "spmm_csr_row_blocks", "spmm_status_string"]
 
 
 class SpmmError(RuntimeError):
@@ -92,6 +92,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "spmm_plan_set_group_lanes": [vp, i32],
         "spmm_plan_set_column_tile": [vp, i32],
         "spmm_pool_release": [],
+        "spmm_check_device": [vp],
+        "spmm_csr_row_blocks": [vp, i32, i32, vp],
         "spmm_status_string": [ctypes.c_int],
     }
     for name, args in sig.items():
@@ -130,8 +132,10 @@ def _ptr(t, dtype, name, allow_none=False):
 
 def _need(t, n, name):
     """Refuse a buffer smaller than the call will read or write (checked before
-    any pointer reaches the library, so a short buffer never becomes an
-    out-of-bounds access on the device)."""
+    any pointer reaches the library).  Every size the call knows on the host
+    is checked this way; the one exception is colind and vals of the one-call
+    forms spmm_csr_f32 / spmm_csr_bf16f32, whose length rowptr[M] exists only
+    on the device (the caller must size them)."""
     if t is not None and t.numel() < n:
         raise ValueError(f"{name} holds {t.numel()} elements; the call needs at least {n}")
 
@@ -201,7 +205,8 @@ def spmm_csr_bf16f32_exec(plan: Plan, K, colind, vals, B, C, stream=None):
 
 
 def _need_one_call(M, K, N, rowptr, B, C):
-    _need(rowptr, M + 1, "rowptr")  # nnz = rowptr[M] is only known on the device
+    # nnz = rowptr[M] is only known on the device: colind and vals are not checked here
+    _need(rowptr, M + 1, "rowptr")
     _need(B, K * N, "B")
     _need(C, M * N, "C")
 
@@ -275,7 +280,11 @@ def spmm_csr_fusedmm_f32(plan: Plan, K, colind, C, B, D, E, stream=None):
 
 
 def spmm_csr_f32_noalloc(M, K, N, nnz, rowptr, colind, vals, B, C, stream=None):
-    """C = A . B (fp32) with the library's fixed scratch array: no allocation anywhere."""
+    """C = A . B (fp32) with the library's fixed scratch array: no allocation anywhere.
+
+    nnz must equal rowptr[M]; the library checks that on the device and
+    reports a mismatch (and any bounded wait that gave up) through
+    ``spmm_check_device``, not through this call's status."""
     _need_one_call(M, K, N, rowptr, B, C)
     _need(colind, nnz, "colind")
     _need(vals, nnz, "vals")
@@ -283,6 +292,24 @@ def spmm_csr_f32_noalloc(M, K, N, nnz, rowptr, colind, vals, B, C, stream=None):
                                        _ptr(vals, _F32, "vals", True), _ptr(B, _F32, "B", True), _ptr(C, _F32, "C"),
                                        _stream(stream)), "spmm_csr_f32_noalloc")
     return C
+
+
+def spmm_check_device(stream=None) -> int:
+    """Synchronise, read and clear the one-call forms' device error word (a status code)."""
+    return load().spmm_check_device(_stream(stream))
+
+
+def spmm_csr_row_blocks(rowptr, parts: int):
+    """First row of each of `parts` row blocks (numpy int32[parts + 1]) for
+    splitting one A over `parts` GPUs; rowptr is a host (numpy) int32 array."""
+    import numpy as np
+    rp = np.ascontiguousarray(rowptr, dtype=np.int32)
+    if rp.ndim != 1 or rp.size < 1:
+        raise ValueError("rowptr must be a 1-D array of M + 1 entries")
+    out = np.empty(max(parts, 0) + 1, dtype=np.int32)
+    _check(load().spmm_csr_row_blocks(ctypes.c_void_p(rp.ctypes.data), rp.size - 1, parts,
+                                      ctypes.c_void_p(out.ctypes.data)), "spmm_csr_row_blocks")
+    return out
 
 
 def spmm_pool_release() -> None:

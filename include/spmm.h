@@ -41,6 +41,16 @@
  *   bitwise-identical C.  The summation order differs from a sequential loop
  *   (rows may be split into pieces that are combined in a fixed order).
  *
+ * Non-finite values
+ *   Inputs are expected to be finite.  The kernels multiply some B rows by a
+ *   zero value instead of skipping them (slots past the end of a row or of a
+ *   batch re-read a valid row with value 0; the window kernels multiply the
+ *   absent entries inside the window), so an Inf or NaN in B can turn into
+ *   NaN: in the row kernel only in a row that references that B row, in the
+ *   nnz-balanced kernel also in a row whose nonzeros share a warp step with
+ *   such a reference, in the window kernels in every row of the block whose
+ *   window holds that B row.
+ *
  * Errors
  *   Every call returns a spmm_status; no exception crosses the ABI and no
  *   kernel traps.  Argument errors are detected before any CUDA call.
@@ -48,7 +58,8 @@
  *   the fast path (undefined results); run spmm_csr_validate to check them.
  *   A CUDA launch or API failure returns SPMM_ERR_CUDA.  Kernels that wait
  *   on hardware copies give up after a bounded time and record
- *   SPMM_ERR_DEVICE_TIMEOUT in the plan, read by spmm_plan_check_device.
+ *   SPMM_ERR_DEVICE_TIMEOUT in the plan, read by spmm_plan_check_device; the
+ *   one-call forms record it in a per-device word read by spmm_check_device.
  */
 #ifndef CSR_SPMM_02_GB300_SPMM_H_
 #define CSR_SPMM_02_GB300_SPMM_H_
@@ -100,13 +111,13 @@ typedef enum {
                               * (tcgen05, accumulator in tensor memory) for bf16 B with
                               * N a multiple of 16 up to 256: a persistent kernel over
                               * 128-row tiles, A's fp32 values split exactly into three
-                              * bf16 terms, B streamed by TMA in 64-row chunks; tiles
-                              * with a span over 192 columns or duplicate columns gather
-                              * per row.  Other B types or widths run the window kernel.
-                              * The three-term split is exact for |vals| >= 2^-110;
-                              * smaller values keep fewer bits (under about 2^-134 they
-                              * are dropped), which can exceed the tolerance for a row
-                              * dominated by such values. */
+                              * bf16 terms (exact for |vals| >= 2^-110), B streamed by
+                              * TMA in 64-row chunks; tiles with a span over 192
+                              * columns, duplicate columns or a nonzero value below
+                              * 2^-110 in magnitude gather per row in fp32.  Other B
+                              * types or widths run the window kernel.  Absent entries
+                              * inside the window are multiplied as zeros, as in the
+                              * window kernel. */
 } spmm_kernel;
 
 /* Opaque plan: owns its device workspace (merge-path partition, carry rows
@@ -251,7 +262,11 @@ SPMM_API spmm_status spmm_csr_fusedmm_f32(spmm_plan_t plan, int32_t K, const int
  * freed blocks reserved for later calls (spmm_pool_release hands them back),
  * so repeated calls map no new memory.  The merge-path partition is built
  * only when the chosen kernel is the balanced one.  For repeated products
- * with the same A, build a plan once and call the _exec form.
+ * with the same A, build a plan once and call the _exec form.  A bounded
+ * wait that gives up in this call's kernels is recorded in the device's
+ * one-call error word (see spmm_check_device), not in the returned status.
+ * colind and vals must hold rowptr[M] entries: the call cannot check their
+ * sizes.
  */
 SPMM_API spmm_status spmm_csr_f32(int32_t M, int32_t K, int32_t N, const int32_t* rowptr,
                          const int32_t* colind, const float* vals, const float* B, float* C,
@@ -288,22 +303,60 @@ SPMM_API spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream);
  * allocator must not be bypassed.
  *
  * It always runs the nnz-balanced kernel and its fixup, with their scratch
- * (range coordinates, carry rows, error word) in one fixed 32 MiB array of
- * device memory that the library itself holds on every device that loads it,
- * until the process exits.  The caller passes all inputs and the output, as
- * for spmm_csr_f32, plus nnz (which must equal rowptr[M]).  A problem whose
- * scratch, about 8 * (P + 1) + 8 * N * P bytes with P = ceil((M + nnz) / 2048),
+ * (range coordinates, carry rows) in one fixed 32 MiB array of device memory
+ * that the library itself holds on every device that loads it, until the
+ * process exits.  The caller passes all inputs and the output, as for
+ * spmm_csr_f32, plus nnz.  A problem whose scratch, 256 + 8 * (P + 1)
+ * (rounded up to 256) + 8 * N * P bytes with P = ceil((M + nnz) / 2048),
  * exceeds the array is rejected with SPMM_ERR_UNSUPPORTED before anything is
- * launched.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and should come before any stream capture on that
- * device.  Every call reuses the same array and leaves its contents behind:
- * calls whose work can overlap on the GPU (other streams, other threads)
- * race; order them.  Asynchronous on `stream`; results are bitwise
- * reproducible for given inputs.
+ * launched.  Every call looks up the array's device address on the current
+ * device (cudaGetSymbolAddress, a host-side lookup); the first call on a
+ * device also loads the library's device code there, so make it before any
+ * stream capture on that device.  Every call reuses the same array and
+ * leaves its contents behind: calls whose work can overlap on the GPU (other
+ * streams, other threads) race; order them.  Asynchronous on `stream`;
+ * results are bitwise reproducible for given inputs.
+ *
+ * nnz must equal rowptr[M].  The call cannot see rowptr[M] without a
+ * synchronisation, so the check runs on the device: on a mismatch no range
+ * reads any nonzero, C is left unwritten and spmm_check_device returns
+ * SPMM_ERR_INVALID_CSR.  A bounded wait that gives up is reported there too
+ * (SPMM_ERR_DEVICE_TIMEOUT).  SPMM_OK from this call means only that the
+ * work was launched: call spmm_check_device to learn whether it completed.
  */
 SPMM_API spmm_status spmm_csr_f32_noalloc(int32_t M, int32_t K, int32_t N, int64_t nnz,
                                           const int32_t* rowptr, const int32_t* colind,
                                           const float* vals, const float* B, float* C, void* stream);
+
+/*
+ * Row-block split of one A over `parts` GPUs (host code; no CUDA call).
+ * `rowptr` is a HOST array of M+1 entries; row_start (host, parts+1 entries,
+ * owned by the caller) receives the first row of every block, row_start[0] =
+ * 0 and row_start[parts] = M.  The merged sequence of nonzeros and row ends
+ * (M + nnz items) is cut into `parts` equal diagonals, as the plan cuts it
+ * into CTA ranges (the even split of nonzeros the Sgap page's related work
+ * credits to Yang et al.), with each row kept whole in the block that holds
+ * its end, so every GPU multiplies the rows row_start[b] .. row_start[b+1]-1
+ * by a replicated B and writes that block of C, with no exchange of partial
+ * rows (the Intel Max page scales one problem over both stacks of its GPU
+ * the same way, with one queue per stack).  A block may be empty when one
+ * row is longer than a whole share.  SPMM_ERR_INVALID_ARG for M < 0,
+ * parts < 1 or a NULL pointer; SPMM_ERR_INVALID_CSR if rowptr[0] != 0 or
+ * rowptr decreases.
+ */
+SPMM_API spmm_status spmm_csr_row_blocks(const int32_t* rowptr, int32_t M, int32_t parts, int32_t* row_start);
+
+/*
+ * Synchronise `stream`, then read and clear the error word that the one-call
+ * forms (spmm_csr_f32, spmm_csr_bf16f32, spmm_csr_f32_noalloc) share on the
+ * current device.  The word collects the bits of every such call on the
+ * device since the last check, whatever its stream.  Returns
+ * SPMM_ERR_INVALID_CSR if a spmm_csr_f32_noalloc call was given an nnz other
+ * than rowptr[M] (that call wrote nothing), else SPMM_ERR_DEVICE_TIMEOUT if a
+ * kernel gave up a bounded wait (its output is incomplete), else SPMM_OK.
+ * Allocates nothing.
+ */
+SPMM_API spmm_status spmm_check_device(void* stream);
 
 /*
  * Optional timing hook.  When `event` (a cudaEvent_t passed as void*) is not

@@ -158,12 +158,14 @@ def test_empty_pattern():
 
 @pytest.mark.parametrize("name", ["uniform64k", "rmat22"])
 def test_workload_structures(name):
-    """Full-size patterns of two benchmark workloads (N of the workload), sampled outputs."""
+    """Full-size patterns of two benchmark workloads (N of the workload): every
+    SDDMM value and every FusedMM output element against the oracles."""
     p = gen.make_workload(name)
     rng = np.random.default_rng(5)
     C = rng.uniform(-1, 1, (p.M, p.N)).astype(np.float32)
     D = rng.uniform(-1, 1, (p.K, p.N)).astype(np.float32)
     B = p.B
+    absD = np.abs(D)
     a = H.device_arrays(p)
     plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N)
     Cd, Bd, Dd = (torch.from_numpy(x).cuda() for x in (C, B, D))
@@ -172,15 +174,18 @@ def test_workload_structures(name):
     E = torch.empty((p.M, p.N), device="cuda")
     spmm.spmm_csr_fusedmm_f32(plan, p.K, a["colind"], Cd, Bd, Dd, E)
     torch.cuda.synchronize()
-    rows = np.unique(np.concatenate([np.argsort(np.diff(p.rowptr))[-32:], rng.choice(p.M, 3000, replace=False)]))
-    sub = gen.CsrProblem("sub", len(rows), p.K, p.N,
-                         np.concatenate([[0], np.cumsum(np.diff(p.rowptr)[rows])]).astype(np.int32),
-                         np.concatenate([p.colind[p.rowptr[r]:p.rowptr[r + 1]] for r in rows]).astype(np.int32),
-                         np.zeros(0, np.float32), B, "f32")
-    sub.vals = np.zeros(len(sub.colind), np.float32)
-    Csub = C[rows]
-    ref, S = oracle.sddmm_reference(sub.rowptr, sub.colind, Csub, B)
-    got = np.concatenate([out[int(p.rowptr[r]):int(p.rowptr[r + 1])].cpu().numpy() for r in rows]).astype(np.float64)
-    assert np.all(np.abs(got - ref) <= 1e-5 * S + 1e-30)
-    Eref, _ = oracle.fusedmm_reference(sub.rowptr, sub.colind, Csub, B, D)
-    H.assert_within(E[torch.from_numpy(rows).cuda()], Eref, fused_bound(sub, Csub, B, D), "f32", name)
+    assert spmm.spmm_plan_check_device(plan) == 0
+    out, E = out.cpu().numpy().astype(np.float64), E.cpu().numpy()
+
+    def block(r0, r1):
+        rp, ci, _ = H.sub_csr(p, r0, r1)
+        ref, S = oracle.sddmm_reference(rp, ci, C[r0:r1], B)
+        Eref, _ = oracle.fusedmm_reference(rp, ci, C[r0:r1], B, D)
+        Sf, _ = oracle.spmm_reference(rp, ci, S.astype(np.float32), absD)
+        return r0, r1, ref, S, Eref, Sf
+
+    for r0, r1, ref, S, Eref, Sf in H.blocks_ahead(block, H.row_blocks(p, 3.0 * p.nnz / p.M * p.N)):
+        got = out[int(p.rowptr[r0]):int(p.rowptr[r1])]
+        bad = np.abs(got - ref) > 1e-5 * S + 1e-30
+        assert not bad.any(), f"{name} sddmm rows {r0}..{r1 - 1}: {int(bad.sum())} values outside the bound"
+        H.assert_within(E[r0:r1], Eref, Sf, "f32", f"{name} fusedmm rows {r0}..{r1 - 1}")

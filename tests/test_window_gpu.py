@@ -175,3 +175,24 @@ def test_tc_deterministic():
     C1, _ = H.run(p, kernel="window_tc")
     C2, _ = H.run(p, kernel="window_tc")
     assert torch.equal(C1, C2)
+
+
+@pytest.mark.parametrize("scale_exp", [-100, -112, -120, -128, -135, -140])
+def test_tc_window_tiny_values(scale_exp):
+    """Rows whose values all lie near 2^scale_exp, next to ordinary rows, on the
+    tensor-core window path.  The three-term bf16 split is exact only for
+    |v| >= 2^-110 (at 2^-128 the hi term is a bf16 subnormal, at 2^-135 and
+    below it rounds to zero), so tiles holding smaller values must take the
+    fp32 gather path; every element must meet the bf16-B bound 8e-3 * S.
+    (Values much below 2^-140 would put exact results in the fp32 subnormal
+    range, where no fp32 output can meet a purely relative bound.)"""
+    p = banded(5, 650, 650, 32, 31, 128, b_dtype="bf16")
+    rng = np.random.default_rng(200 - scale_exp)
+    tiny_rows = [0, 1, 130, 131, 300, 645]  # rows of several 128-row tiles, incl. the ragged last one
+    for r in tiny_rows:
+        a, b = int(p.rowptr[r]), int(p.rowptr[r + 1])
+        assert b > a
+        mant = rng.uniform(1.0, 2.0, b - a) * rng.choice([-1.0, 1.0], b - a)
+        p.vals[a:b] = (mant * 2.0 ** scale_exp).astype(np.float32)
+    _, info = check(p, kernel="auto")
+    assert info["kernel"] == "window_tc"
