@@ -36,6 +36,11 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// cudaErrorNotSupported from a launch: a size the kernels cannot address.
+spmm_status status_of(cudaError_t e) {
+  return e == cudaSuccess ? SPMM_OK : e == cudaErrorNotSupported ? SPMM_ERR_UNSUPPORTED : SPMM_ERR_CUDA;
+}
+
 struct DeviceGuard {  // run on the plan's device, restore the caller's afterwards
   int prev = -1;
   bool ok = true;
@@ -104,7 +109,7 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
     if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
     if (e == cudaSuccess) e = launch_fixup(L);
   }
-  return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+  return status_of(e);
 }
 
 Launch plan_launch(spmm_plan_t plan, cudaStream_t stream) {
@@ -181,7 +186,7 @@ spmm_status semiring(spmm_plan_t plan, int32_t K, const int32_t* colind, const f
   cudaError_t e = launch_semiring_f32(L, cap_tile(choose_shape_balanced(plan->N, false, vector_ok), plan->column_tile), sr);
   if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
   if (e == cudaSuccess) e = launch_fixup(L, sr);
-  return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+  return status_of(e);
 }
 
 spmm_status fusedmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* Cd, const float* B,
@@ -296,6 +301,7 @@ const char* spmm_status_string(spmm_status status) {
     case SPMM_ERR_PLAN_MISMATCH: return "SPMM_ERR_PLAN_MISMATCH";
     case SPMM_ERR_CUDA: return "SPMM_ERR_CUDA";
     case SPMM_ERR_DEVICE_TIMEOUT: return "SPMM_ERR_DEVICE_TIMEOUT";
+    case SPMM_ERR_OUT_OF_BOUNDS: return "SPMM_ERR_OUT_OF_BOUNDS";
   }
   return "SPMM_ERR_UNKNOWN";
 }

@@ -172,11 +172,22 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>
   } else {
     for (int g = i0 + tid; g <= i1; g += kThreads) s_rp[g - rbase] = ld_stream(rowptr + g, stream_pol);
   }
-  const bool staged = mbar_wait_bounded(bar, 0, kSpinLimit);
+  // (the test build's limit of one poll takes a single non-blocking look)
+  const bool staged = kStageSpinLimit <= 1 ? mbar_test(bar, 0) : mbar_wait_bounded(bar, 0, kStageSpinLimit);
   if (__syncthreads_or(!staged)) {
     if (tid == 0) atomicOr(err, kErrStageTimeout);
     mbar_wait_bounded(bar, 0, kSpinLimit);  // let copies in flight land before leaving
     return;
+  }
+  // SpMM: column indices become the offsets of their B rows in VEC-element
+  // units (c * N / VEC < 2^32, which the launch checks), so that a gather's
+  // address is one multiply-add on a 32-bit offset (rmat22 826 -> 818 us,
+  // rmat20 543 -> 525 us).  FusedMM keeps the column indices: its extra
+  // registers for the offsets spilled and cost more than they saved.
+  if constexpr (!FUSED) {
+    const uint32_t nv = uint32_t(N / VEC);
+    for (int k = p0 - nbase + tid; k < p1 - nbase; k += kThreads) s_col[k] = int(uint32_t(s_col[k]) * nv);
+    __syncthreads();
   }
 
   // ---- 2. this warp's sub-range ---------------------------------------------
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>
     float fv[FUSED ? U : 1];
 #pragma unroll
     for (int s = 0; s < U; ++s) {  // gathers first
-      const size_t roff = size_t(colw[q + s * S]) * N;
+      const size_t roff = FUSED ? size_t(colw[q + s * S]) * N : size_t(uint32_t(colw[q + s * S])) * VEC;
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
       if constexpr (FUSED) load_dot(q + s * S + grp - nbase, bd[s], cd[s]);
@@ -397,7 +408,8 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>
     float fv[FUSED ? U : 1];
 #pragma unroll
     for (int s = 0; s < U; ++s) {
-      const size_t roff = size_t(colw[min(q + s * S, pw1 - 1 - grp)]) * N;
+      const int c = colw[min(q + s * S, pw1 - 1 - grp)];
+      const size_t roff = FUSED ? size_t(c) * N : size_t(uint32_t(c)) * VEC;
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
       if constexpr (FUSED) load_dot(min(q + s * S + grp, pw1 - 1) - nbase, bd[s], cd[s]);
@@ -470,7 +482,14 @@ cudaError_t launch_balanced_t(const Launch& L, const float* Cd = nullptr, const 
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
+  // SpMM keeps B-row offsets in 32 bits (VEC-element units): column c's row
+  // starts c * N / VEC vectors into B.
+  if (!FUSED && int64_t(L.K) * (L.N / VEC) > int64_t(UINT32_MAX)) return cudaErrorNotSupported;
   const dim3 grid(unsigned(L.num_ctas), unsigned((L.N + TW - 1) / TW));
+  SPMM_DEBUG_RANGES(L.stream, L.err,
+                    {{L.B, size_t(L.K) * L.N * sizeof(BT)}, {Cd, FUSED ? size_t(L.M) * L.N * 4 : 0},
+                     {Bd, FUSED ? size_t(L.K) * L.N * 4 : 0}},
+                    {{L.C, size_t(L.M) * L.N * 4}, {L.carry, size_t(L.num_ctas) * 2 * L.N * 4}});
   spmm_balanced_kernel<BT, VEC, G, NCH, FUSED, SR><<<grid, kThreads, smem, L.stream>>>(
       L.M, L.N, L.rowptr, L.colind, L.vals, static_cast<const BT*>(L.B), L.C, L.part,
       L.items_per_cta, L.carry, L.err, Cd, Bd);

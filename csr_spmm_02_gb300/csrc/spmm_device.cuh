@@ -12,6 +12,8 @@
 #pragma once
 
 #include <cstdint>
+#include <initializer_list>
+
 #include <cuda_runtime.h>
 
 namespace spmm {
@@ -19,11 +21,94 @@ namespace spmm {
 constexpr int kThreads = 256;           // threads per CTA for every SpMM kernel
 constexpr uint32_t kSpinLimit = 1u << 22;  // bound on mbarrier polls before giving up
 
+// Device error word bits.
+constexpr int kErrStageTimeout = 1;  // a bounded wait gave up
+constexpr int kErrInvalidCsr = 2;    // rowptr[M] differs from the nnz the caller passed
+constexpr int kErrBounds = 4;        // (bounds-checked build) an access outside its buffers was skipped
+
+// The first wait of a kernel for its staged copies.  A test build lowers it
+// (SPMM_STAGE_SPIN_LIMIT=1: one non-blocking look) to make that wait give up
+// while the copies are still in flight; the kernel then still waits
+// (kSpinLimit) for them to land before it leaves.
+#ifndef SPMM_STAGE_SPIN_LIMIT
+#define SPMM_STAGE_SPIN_LIMIT kSpinLimit
+#endif
+constexpr uint32_t kStageSpinLimit = SPMM_STAGE_SPIN_LIMIT;
+
 #ifndef SPMM_L2_HINTS
 #define SPMM_L2_HINTS 1  // stream A and C with evict-first so B's reused rows stay in L2
 #endif
 #ifndef SPMM_B_EVICT_LAST
 #define SPMM_B_EVICT_LAST 0  // give B gathers evict-last priority in L2
+#endif
+
+// ---------------------------------------------------------------------------
+// Bounds-checked build (-DSPMM_DEBUG_BOUNDS): every B-row gather
+// (BSlice::load, the row kernel's policy loads, the window kernel's cp.async
+// staging of B rows) and every C / output store (st_stream4, st_stream1,
+// st_plain1) checks its address against the buffers the launch registered;
+// an access outside them is skipped and kErrBounds is set in the launch's
+// error word.  Nothing traps: the kernel runs to its end and the host reads
+// the word.  The ranges live in a per-translation-unit __device__ variable
+// that each launch wrapper fills on the launch stream before its launch.
+// ---------------------------------------------------------------------------
+#ifdef SPMM_DEBUG_BOUNDS
+struct DebugRanges {
+  uint64_t load_lo[3], load_hi[3];    // buffers gathered from
+  uint64_t store_lo[2], store_hi[2];  // buffers stored to
+  int* err;
+};
+static __device__ DebugRanges g_debug_ranges;
+
+__device__ __forceinline__ bool debug_access_ok(const void* p, int bytes, const uint64_t* lo, const uint64_t* hi,
+                                                int n) {
+  const uint64_t a = reinterpret_cast<uint64_t>(p);
+  for (int k = 0; k < n; ++k)
+    if (a >= lo[k] && a + uint64_t(bytes) <= hi[k]) return true;
+  if (g_debug_ranges.err) atomicOr(g_debug_ranges.err, kErrBounds);
+  return false;
+}
+__device__ __forceinline__ bool debug_load_ok(const void* p, int bytes) {
+  return debug_access_ok(p, bytes, g_debug_ranges.load_lo, g_debug_ranges.load_hi, 3);
+}
+__device__ __forceinline__ bool debug_store_ok(const void* p, int bytes) {
+  return debug_access_ok(p, bytes, g_debug_ranges.store_lo, g_debug_ranges.store_hi, 2);
+}
+
+struct DebugBuffer {
+  const void* p;
+  size_t bytes;
+};
+// Register the buffers of the next launch on `s` (up to three gathered, two stored).
+static inline cudaError_t debug_ranges(cudaStream_t s, int* err, std::initializer_list<DebugBuffer> loads,
+                                       std::initializer_list<DebugBuffer> stores) {
+  DebugRanges h{};
+  int k = 0;
+  for (const DebugBuffer& b : loads) {
+    h.load_lo[k] = reinterpret_cast<uint64_t>(b.p);
+    h.load_hi[k] = h.load_lo[k] + (b.p ? b.bytes : 0);
+    ++k;
+  }
+  k = 0;
+  for (const DebugBuffer& b : stores) {
+    h.store_lo[k] = reinterpret_cast<uint64_t>(b.p);
+    h.store_hi[k] = h.store_lo[k] + (b.p ? b.bytes : 0);
+    ++k;
+  }
+  h.err = err;
+  return cudaMemcpyToSymbolAsync(g_debug_ranges, &h, sizeof h, 0, cudaMemcpyHostToDevice, s);
+}
+#define SPMM_DEBUG_LOAD_GUARD(p, bytes, on_fail) \
+  if (!debug_load_ok(p, bytes)) { on_fail; return; }
+#define SPMM_DEBUG_STORE_GUARD(p, bytes) \
+  if (!debug_store_ok(p, bytes)) return;
+#define SPMM_DEBUG_RANGES(...) \
+  do { const cudaError_t de_ = debug_ranges(__VA_ARGS__); if (de_ != cudaSuccess) return de_; } while (0)
+#else
+#define SPMM_DEBUG_LOAD_GUARD(p, bytes, on_fail)
+#define SPMM_DEBUG_STORE_GUARD(p, bytes)
+#define SPMM_DEBUG_RANGES(...) \
+  do { } while (0)
 #endif
 
 // ---------------------------------------------------------------------------
@@ -121,7 +206,10 @@ struct BSlice;
 template <>
 struct BSlice<float, 4> {
   float4 r;
-  __device__ __forceinline__ void load(const float* p) { r = __ldg(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ void load(const float* p) {
+    SPMM_DEBUG_LOAD_GUARD(p, 16, r = make_float4(0.f, 0.f, 0.f, 0.f))
+    r = __ldg(reinterpret_cast<const float4*>(p));
+  }
   __device__ __forceinline__ void load_shared(const float* p) { r = *reinterpret_cast<const float4*>(p); }
   __device__ __forceinline__ void widen(FVec<4>& o) const {
     o.p[0] = make_float2(r.x, r.y);
@@ -132,7 +220,10 @@ struct BSlice<float, 4> {
 template <>
 struct BSlice<float, 1> {
   float r;
-  __device__ __forceinline__ void load(const float* p) { r = __ldg(p); }
+  __device__ __forceinline__ void load(const float* p) {
+    SPMM_DEBUG_LOAD_GUARD(p, 4, r = 0.f)
+    r = __ldg(p);
+  }
   __device__ __forceinline__ void widen(FVec<1>& o) const { o.x = r; }
 };
 
@@ -143,7 +234,10 @@ __device__ __forceinline__ float2 bf16x2_widen(uint32_t w) {
 template <>
 struct BSlice<uint16_t, 8> {
   uint4 r;
-  __device__ __forceinline__ void load(const uint16_t* p) { r = __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ __forceinline__ void load(const uint16_t* p) {
+    SPMM_DEBUG_LOAD_GUARD(p, 16, r = make_uint4(0u, 0u, 0u, 0u))
+    r = __ldg(reinterpret_cast<const uint4*>(p));
+  }
   __device__ __forceinline__ void load_shared(const uint16_t* p) { r = *reinterpret_cast<const uint4*>(p); }
   __device__ __forceinline__ void widen(FVec<8>& o) const {
     o.p[0] = bf16x2_widen(r.x);
@@ -156,7 +250,10 @@ struct BSlice<uint16_t, 8> {
 template <>
 struct BSlice<uint16_t, 1> {
   unsigned short r;
-  __device__ __forceinline__ void load(const uint16_t* p) { r = __ldg(reinterpret_cast<const unsigned short*>(p)); }
+  __device__ __forceinline__ void load(const uint16_t* p) {
+    SPMM_DEBUG_LOAD_GUARD(p, 2, r = 0)
+    r = __ldg(reinterpret_cast<const unsigned short*>(p));
+  }
   __device__ __forceinline__ void widen(FVec<1>& o) const { o.x = __uint_as_float(uint32_t(r) << 16); }
 };
 
@@ -235,6 +332,7 @@ __device__ __forceinline__ void sr_combine_shfl_xor(FVec<VEC>& a, int mask) {
 // C stores (each C element is written once: streaming / evict-first)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void st_stream4(float* p, float x, float y, float z, float w) {
+  SPMM_DEBUG_STORE_GUARD(p, 16)
 #if SPMM_L2_HINTS
   asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "f"(x), "f"(y), "f"(z), "f"(w),
                "l"(policy_evict_first())
@@ -244,11 +342,18 @@ __device__ __forceinline__ void st_stream4(float* p, float x, float y, float z, 
 #endif
 }
 __device__ __forceinline__ void st_stream1(float* p, float x) {
+  SPMM_DEBUG_STORE_GUARD(p, 4)
 #if SPMM_L2_HINTS
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(x), "l"(policy_evict_first()) : "memory");
 #else
   __stcs(p, x);
 #endif
+}
+
+// A plain (write-back) store of one output value.
+__device__ __forceinline__ void st_plain1(float* p, float x) {
+  SPMM_DEBUG_STORE_GUARD(p, 4)
+  *p = x;
 }
 
 template <int VEC>
@@ -293,6 +398,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 #endif
 }
 
+// One non-blocking look at the barrier's phase `parity` (test_wait never
+// suspends the thread, unlike try_wait); true when it has completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Poll the barrier's phase `parity` at most `limit` times; true when it completed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit) {
   for (uint32_t it = 0; it < limit; ++it) {
@@ -309,8 +428,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   return false;
 }
 
-// Device error word bits.
-constexpr int kErrStageTimeout = 1;  // a bounded wait gave up
-constexpr int kErrInvalidCsr = 2;    // rowptr[M] differs from the nnz the caller passed
+
 
 }  // namespace spmm

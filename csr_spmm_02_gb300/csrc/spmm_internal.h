@@ -40,7 +40,6 @@ struct spmm_plan_s {
   int32_t group_lanes = 0;    // SMALLN only: lanes sharing a row
   int32_t column_tile = 0;    // N-slicing cap of the row and balanced kernels (0: none)
   int device = 0;
-  bool stream_ordered = false;  // workspace from cudaMallocAsync (one-call form)
   // device workspace (one allocation, carved up)
   void* workspace = nullptr;
   int64_t workspace_bytes = 0;
@@ -107,6 +106,8 @@ cudaError_t launch_tc_window_bf16(const Launch& L);
 cudaError_t launch_window_f32(const Launch& L);
 cudaError_t launch_window_bf16(const Launch& L);
 cudaError_t launch_fixup(const Launch& L, int sr = 0);  // sr: semiring code, 0 = sum
+// The balanced SpMM kernels (ordinary and semiring) return
+// cudaErrorNotSupported when K * N / VEC does not fit 32 bits.
 // Balanced kernel with a semiring (fp32 B); sr = 2 * add + mul in 1..5
 // (add 0 sum, 1 min, 2 max; mul 0 multiply, 1 add).
 cudaError_t launch_semiring_f32(const Launch& L, Shape s, int sr);

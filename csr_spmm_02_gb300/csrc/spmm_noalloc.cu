@@ -112,7 +112,7 @@ extern "C" SPMM_API spmm_status spmm_csr_f32_noalloc(int32_t M, int32_t K, int32
   L.stream = s;
   cudaError_t e = launch_balanced_f32(L, choose_shape_balanced(N, false, vector_ok));
   if (e == cudaSuccess) e = launch_fixup(L);
-  return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+  return e == cudaSuccess ? SPMM_OK : e == cudaErrorNotSupported ? SPMM_ERR_UNSUPPORTED : SPMM_ERR_CUDA;
 }
 
 extern "C" SPMM_API spmm_status spmm_check_device(void* stream) {
@@ -124,6 +124,7 @@ extern "C" SPMM_API spmm_status spmm_check_device(void* stream) {
   if (cudaMemsetAsync(word, 0, sizeof host, s) != cudaSuccess) return SPMM_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return SPMM_ERR_CUDA;
   if (host & spmm::kErrInvalidCsr) return SPMM_ERR_INVALID_CSR;
+  if (host & spmm::kErrBounds) return SPMM_ERR_OUT_OF_BOUNDS;
   if (host & spmm::kErrStageTimeout) return SPMM_ERR_DEVICE_TIMEOUT;
   return SPMM_OK;
 }

@@ -10,22 +10,51 @@
 
 namespace spmm {
 
-// stats[0] = longest row, stats[1] = number of empty rows, stats[2] = rowptr[M].
-__global__ void __launch_bounds__(kThreads) row_stats_kernel(const int32_t* __restrict__ rowptr, int32_t M,
-                                                             int* __restrict__ stats) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) stats[2] = __ldg(rowptr + M);
+// One pass over rowptr.  stats[0] = longest row, stats[1] = number of empty
+// rows, stats[2] = rowptr[M] (block-reduced, one atomic per block).  With
+// part: the merge-path coordinates of the P+1 range starts, found without a
+// search: row i's end item sits at e(i) = rowptr[i+1] + i, so the diagonals
+// c*T with e(i-1) < c*T <= e(i) start inside row i, at nonzero c*T - i;
+// part[P] = (M, nnz) closes the sequence.  nnz and P are the caller's (a
+// rowptr[M] that differs is caught from stats[2] on the host; no index past
+// part[P] is written either way).
+__global__ void __launch_bounds__(kThreads) plan_rows_kernel(const int32_t* __restrict__ rowptr, int32_t M,
+                                                             int64_t nnz, int64_t T, int32_t P,
+                                                             int* __restrict__ stats, int2* __restrict__ part) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    stats[2] = __ldg(rowptr + M);
+    if (part) part[P] = make_int2(M, int(nnz));
+  }
   int longest = 0, empty = 0;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < M; i += int64_t(gridDim.x) * blockDim.x) {
-    const int len = __ldg(rowptr + i + 1) - __ldg(rowptr + i);
+    const int a = __ldg(rowptr + i), b = __ldg(rowptr + i + 1);
+    const int len = b - a;
     longest = max(longest, len);
     empty += len == 0;
+    if (part) {
+      const int64_t prev_end = int64_t(a) + i - 1;  // e(i-1); -1 for the first row
+      const int64_t c0 = prev_end < 0 ? 0 : prev_end / T + 1;
+      const int64_t c1 = min((int64_t(b) + i) / T, int64_t(P) - 1);
+      for (int64_t c = c0; c <= c1; ++c) part[c] = make_int2(int(i), int(c * T - i));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
     empty += __shfl_xor_sync(0xffffffffu, empty, o);
   }
+  __shared__ int s_long[kThreads / 32], s_empty[kThreads / 32];
+  const int w = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) {
+    s_long[w] = longest;
+    s_empty[w] = empty;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < kThreads / 32; ++k) {
+      longest = max(longest, s_long[k]);
+      empty += s_empty[k];
+    }
     atomicMax(stats, longest);
     atomicAdd(stats + 1, empty);
   }
@@ -78,11 +107,14 @@ __global__ void __launch_bounds__(kThreads) validate_kernel(const int32_t* __res
 // One warp per CTA range c.  If a row starts inside range c and its end item
 // lies in a later range (carry slot 1 of c), add slot 1 of c and slot 0 of
 // every following range up to the one holding the row's end, in range order,
-// and write the C row.  SR: the semiring whose (+) combines the pieces.
+// and write the C row.  The ranges are T items each, so the range holding the
+// row's end item (position rowptr[row+1] + row) follows from rowptr alone and
+// every carry load of the row can be in flight at once.  SR: the semiring
+// whose (+) combines the pieces.
 template <int SR>
 __global__ void __launch_bounds__(kThreads) spmm_fixup_kernel(int32_t M, int32_t N,
                                                               const int32_t* __restrict__ rowptr,
-                                                              const int2* __restrict__ part, int32_t P,
+                                                              const int2* __restrict__ part, int32_t P, int32_t T,
                                                               const float* __restrict__ carry,
                                                               float* __restrict__ C) {
   const int c = blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
@@ -94,11 +126,18 @@ __global__ void __launch_bounds__(kThreads) spmm_fixup_kernel(int32_t M, int32_t
   if (row >= M) return;
   const int rs = __ldg(rowptr + row);
   if (rs < beg.y || rs >= fin.y) return;  // the row does not start inside range c
-  int last = c + 1;
-  while (__ldg(part + last + 1).x == row) ++last;  // range `last` holds the row's end item
+  const int last = int((int64_t(__ldg(rowptr + row + 1)) + row) / T);  // range holding the row's end item
   for (int n = lane; n < N; n += 32) {
-    float s = carry[(size_t(c) * 2 + 1) * N + n];
-    for (int c2 = c + 1; c2 <= last; ++c2) s = sr_plus<SR>(s, carry[(size_t(c2) * 2) * N + n]);
+    float s = __ldcg(carry + (size_t(c) * 2 + 1) * N + n);
+    constexpr int kAhead = 8;  // slot loads in flight per lane
+    for (int c0 = c + 1; c0 <= last; c0 += kAhead) {
+      float v[kAhead];
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k) v[k] = c0 + k <= last ? __ldcg(carry + (size_t(c0 + k) * 2) * N + n) : 0.f;
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k)
+        if (c0 + k <= last) s = sr_plus<SR>(s, v[k]);
+    }
     st_stream1(C + size_t(row) * N + n, s);
   }
 }
@@ -106,9 +145,10 @@ __global__ void __launch_bounds__(kThreads) spmm_fixup_kernel(int32_t M, int32_t
 cudaError_t launch_fixup(const Launch& L, int sr) {
   constexpr int kWarps = kThreads / 32;
   const unsigned grid = unsigned((L.num_ctas + kWarps - 1) / kWarps);
+  SPMM_DEBUG_RANGES(L.stream, L.err, {}, {{L.C, size_t(L.M) * L.N * 4}});
   switch (sr) {
 #define SPMM_FIXUP_CASE(X) \
-  case X: spmm_fixup_kernel<X><<<grid, kThreads, 0, L.stream>>>(L.M, L.N, L.rowptr, L.part, L.num_ctas, L.carry, L.C); break;
+  case X: spmm_fixup_kernel<X><<<grid, kThreads, 0, L.stream>>>(L.M, L.N, L.rowptr, L.part, L.num_ctas, L.items_per_cta, L.carry, L.C); break;
     SPMM_FIXUP_CASE(0) SPMM_FIXUP_CASE(1) SPMM_FIXUP_CASE(2) SPMM_FIXUP_CASE(3) SPMM_FIXUP_CASE(4) SPMM_FIXUP_CASE(5)
 #undef SPMM_FIXUP_CASE
     default: return cudaErrorInvalidValue;
@@ -129,14 +169,14 @@ using namespace spmm;
 
 namespace {
 
-// The one-call forms allocate from a pool of their own on each device, with
-// the release threshold raised so that freed blocks stay reserved for the
-// next call.  (The device's default pool returns its memory to the system at
+// Plans (and so the one-call forms) allocate from a pool of the library's
+// own on each device, with the release threshold raised so that freed blocks
+// stay reserved for the next plan.  (The device's default pool returns its memory to the system at
 // every synchronisation, and mapping it again costs about 0.1 ms per call.)
 std::mutex g_pool_mutex;
 cudaMemPool_t g_pool[kMaxDevices] = {};
 
-cudaError_t one_call_pool(cudaMemPool_t* out) {
+cudaError_t library_pool(cudaMemPool_t* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -160,15 +200,15 @@ cudaError_t one_call_pool(cudaMemPool_t* out) {
   return cudaSuccess;
 }
 
-cudaError_t dev_alloc(void** p, size_t bytes, bool stream_ordered, cudaStream_t s) {
-  if (!stream_ordered) return cudaMalloc(p, bytes);
+// Stream-ordered allocation on `s` from the library's pool (cheap once the
+// pool holds enough; no device-wide synchronisation).
+cudaError_t dev_alloc(void** p, size_t bytes, cudaStream_t s) {
   cudaMemPool_t pool = nullptr;
-  const cudaError_t e = one_call_pool(&pool);
+  const cudaError_t e = library_pool(&pool);
   return e == cudaSuccess ? cudaMallocFromPoolAsync(p, bytes, pool, s) : e;
 }
-void dev_free(void* p, bool stream_ordered, cudaStream_t s) {
-  if (!p) return;
-  if (stream_ordered) cudaFreeAsync(p, s); else cudaFree(p);
+void dev_free(void* p, cudaStream_t s) {
+  if (p) cudaFreeAsync(p, s);
 }
 
 unsigned stats_grid(int32_t M) {
@@ -199,7 +239,6 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   plan->nnz = std::max<int64_t>(nnz, 0);
   plan->N = N;
   plan->rowptr = rowptr;
-  plan->stream_ordered = one_call;
   plan->kernel = kernel == SPMM_KERNEL_AUTO ? SPMM_KERNEL_ROW : kernel;
   if (cudaGetDevice(&plan->device) != cudaSuccess) {
     delete plan;
@@ -211,19 +250,45 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   }
 
   auto fail = [&](spmm_status st) {
-    dev_free(plan->workspace, one_call, stream);
-    dev_free(plan->small, one_call, stream);
+    dev_free(plan->workspace, stream);
+    dev_free(plan->small, stream);
     delete plan;
     return st;
   };
 
+  // The plan form knows nnz up front: the workspace is allocated first and
+  // one pass over rowptr computes the statistics and the merge-path
+  // partition together (one launch, one synchronisation).  The one-call
+  // forms learn nnz from that pass and build the partition afterwards, only
+  // when the balanced kernel is chosen.
+  const int T = items_per_cta ? items_per_cta : default_items_per_cta(N);
+  auto carve = [&](int64_t P) -> spmm_status {  // partition + carry rows for P ranges
+    if (P > INT32_MAX - 1) return SPMM_ERR_UNSUPPORTED;
+    plan->items_per_cta = T;
+    plan->num_ctas = int32_t(P);
+    const size_t part_bytes = (size_t(P) + 1) * sizeof(int2);
+    const size_t part_padded = (part_bytes + 255) & ~size_t(255);
+    const size_t carry_bytes = size_t(P) * 2 * size_t(N) * sizeof(float);
+    plan->workspace_bytes = int64_t(part_padded + carry_bytes);
+    if (dev_alloc(&plan->workspace, part_padded + carry_bytes, stream) != cudaSuccess) return SPMM_ERR_CUDA;
+    plan->part = static_cast<int2*>(plan->workspace);
+    plan->carry = reinterpret_cast<float*>(static_cast<char*>(plan->workspace) + part_padded);
+    return SPMM_OK;
+  };
+  const int64_t P_known = one_call ? 0 : (int64_t(M) + nnz + T - 1) / T;
+  if (!one_call) {
+    const spmm_status st = carve(P_known);
+    if (st != SPMM_OK) return fail(st);
+  }
+
   // error word + statistics (16 bytes)
-  cudaError_t e = dev_alloc(&plan->small, 16, one_call, stream);
+  cudaError_t e = dev_alloc(&plan->small, 16, stream);
   if (e != cudaSuccess) return fail(SPMM_ERR_CUDA);
   plan->err = static_cast<int*>(plan->small);
   plan->stats = plan->err + 1;
   if ((e = cudaMemsetAsync(plan->small, 0, 16, stream)) != cudaSuccess) return fail(SPMM_ERR_CUDA);
-  row_stats_kernel<<<stats_grid(M), kThreads, 0, stream>>>(rowptr, M, plan->stats);
+  plan_rows_kernel<<<stats_grid(M), kThreads, 0, stream>>>(rowptr, M, std::max<int64_t>(nnz, 0), T, int32_t(P_known),
+                                                           plan->stats, plan->part);
   if ((e = cudaGetLastError()) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   int host_stats[3] = {0, 0, 0};
   if ((e = cudaMemcpyAsync(host_stats, plan->stats, sizeof host_stats, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
@@ -256,25 +321,13 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
     plan->group_lanes = r;
   }
 
-  // merge-path partition and carry rows: used by the balanced SpMM, SDDMM and
-  // FusedMM (a one-call SpMM on another kernel needs neither)
-  if (!one_call || plan->kernel == SPMM_KERNEL_BALANCED) {
-    const int T = items_per_cta ? items_per_cta : default_items_per_cta(N);
-    const int64_t total = int64_t(M) + nnz;
-    const int64_t P = (total + T - 1) / T;
-    if (P > INT32_MAX - 1) return fail(SPMM_ERR_UNSUPPORTED);
-    plan->items_per_cta = T;
-    plan->num_ctas = int32_t(P);
-    const size_t part_bytes = (size_t(P) + 1) * sizeof(int2);
-    const size_t part_padded = (part_bytes + 255) & ~size_t(255);
-    const size_t carry_bytes = size_t(P) * 2 * size_t(N) * sizeof(float);
-    plan->workspace_bytes = int64_t(part_padded + carry_bytes);
-    if ((e = dev_alloc(&plan->workspace, part_padded + carry_bytes, one_call, stream)) != cudaSuccess)
-      return fail(SPMM_ERR_CUDA);
-    plan->part = static_cast<int2*>(plan->workspace);
-    plan->carry = reinterpret_cast<float*>(static_cast<char*>(plan->workspace) + part_padded);
-    const unsigned grid = unsigned((P + 1 + kThreads - 1) / kThreads);
-    merge_path_partition_kernel<<<grid, kThreads, 0, stream>>>(rowptr, M, nnz, T, int32_t(P), plan->part, nullptr);
+  // one-call forms: the merge-path partition and carry rows, only for the
+  // balanced kernel (a one-call SpMM on another kernel needs neither)
+  if (one_call && plan->kernel == SPMM_KERNEL_BALANCED) {
+    const int64_t P = (int64_t(M) + nnz + T - 1) / T;
+    const spmm_status st = carve(P);
+    if (st != SPMM_OK) return fail(st);
+    plan_rows_kernel<<<stats_grid(M), kThreads, 0, stream>>>(rowptr, M, nnz, T, int32_t(P), plan->stats, plan->part);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   }
   plan->workspace_bytes += 16;
@@ -284,8 +337,8 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
 
 void spmm_free_plan(spmm_plan_t plan, cudaStream_t stream) {
   if (!plan) return;
-  dev_free(plan->workspace, plan->stream_ordered, stream);
-  dev_free(plan->small, plan->stream_ordered, stream);
+  dev_free(plan->workspace, stream);
+  dev_free(plan->small, stream);
   delete plan;
 }
 
@@ -335,7 +388,7 @@ spmm_status spmm_plan_set_group_lanes(spmm_plan_t plan, int32_t lanes) {
 
 spmm_status spmm_plan_destroy(spmm_plan_t plan) {
   if (!plan) return SPMM_OK;
-  if (plan->stream_ordered) cudaDeviceSynchronize();
+  cudaDeviceSynchronize();  // the plan may be in use on any stream
   spmm_free_plan(plan, nullptr);
   return SPMM_OK;
 }
@@ -348,6 +401,7 @@ spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream) {
   if (cudaMemcpyAsync(&word, plan->err, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SPMM_ERR_CUDA;
   if (cudaMemsetAsync(plan->err, 0, sizeof word, s) != cudaSuccess) return SPMM_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return SPMM_ERR_CUDA;
+  if (word & kErrBounds) return SPMM_ERR_OUT_OF_BOUNDS;
   return word ? SPMM_ERR_DEVICE_TIMEOUT : SPMM_OK;
 }
 
@@ -358,7 +412,7 @@ spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int3
   if (!rowptr || (nnz > 0 && !colind)) return SPMM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* flag = nullptr;
-  if (dev_alloc(reinterpret_cast<void**>(&flag), sizeof(int), true, s) != cudaSuccess) return SPMM_ERR_CUDA;
+  if (dev_alloc(reinterpret_cast<void**>(&flag), sizeof(int), s) != cudaSuccess) return SPMM_ERR_CUDA;
   int host = 0;
   cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(int), s);
   if (e == cudaSuccess) {
@@ -368,7 +422,7 @@ spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int3
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = cudaMemcpyAsync(&host, flag, sizeof(int), cudaMemcpyDeviceToHost, s);
-  dev_free(flag, true, s);
+  dev_free(flag, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return SPMM_ERR_CUDA;
   return host ? SPMM_ERR_INVALID_CSR : SPMM_OK;

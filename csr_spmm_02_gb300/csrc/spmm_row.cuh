@@ -46,6 +46,9 @@ struct RowTiling {
 // loaded are those of BSlice::load).
 __device__ __forceinline__ uint4 ld_b16_policy(const void* p, uint64_t pol) {
   uint4 v;
+#ifdef SPMM_DEBUG_BOUNDS
+  if (!debug_load_ok(p, 16)) return make_uint4(0u, 0u, 0u, 0u);
+#endif
   asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p), "l"(pol));
@@ -216,6 +219,7 @@ cudaError_t launch_row_t(const Launch& L) {
   const int64_t need = (int64_t(L.M) + kGroups - 1) / kGroups;
   const int64_t wave = std::max<int64_t>(1, row_blocks_per_sm<BT, VEC, G, NCH>(dev) / int64_t(tiles));
   const dim3 grid(unsigned(std::min(need, wave)), tiles);
+  SPMM_DEBUG_RANGES(L.stream, L.err, {{L.B, size_t(L.K) * L.N * sizeof(BT)}}, {{L.C, size_t(L.M) * L.N * 4}});
   spmm_row_kernel<BT, VEC, G, NCH><<<grid, kThreads, 0, L.stream>>>(
       L.M, L.N, L.rowptr, L.colind, L.vals, static_cast<const BT*>(L.B), L.C);
   return cudaGetLastError();

@@ -94,6 +94,7 @@ template <typename BT, int VEC, int NCH, int R>
 cudaError_t launch_rowgroup_t(const Launch& L) {
   constexpr int kRowsPerCta = kThreads / R;
   const unsigned grid = unsigned((int64_t(L.M) + kRowsPerCta - 1) / kRowsPerCta);
+  SPMM_DEBUG_RANGES(L.stream, L.err, {{L.B, size_t(L.K) * L.N * sizeof(BT)}}, {{L.C, size_t(L.M) * L.N * 4}});
   spmm_rowgroup_kernel<BT, VEC, NCH, R><<<grid, kThreads, 0, L.stream>>>(
       L.M, L.N, L.rowptr, L.colind, L.vals, static_cast<const BT*>(L.B), L.C);
   return cudaGetLastError();

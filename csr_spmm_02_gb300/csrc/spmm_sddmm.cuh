@@ -278,6 +278,8 @@ cudaError_t launch_sddmm_t(const Launch& L, const float* Cd, float* out) {
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
+  SPMM_DEBUG_RANGES(L.stream, L.err, {{L.B, size_t(L.K) * L.N * 4}, {Cd, size_t(L.M) * L.N * 4}},
+                    {{out, size_t(L.nnz) * 4}});
   spmm_sddmm_kernel<VEC, G, NCH><<<unsigned(L.num_ctas), kThreads, smem, L.stream>>>(
       L.M, L.N, L.rowptr, L.colind, Cd, static_cast<const float*>(L.B), out, L.part, L.items_per_cta, L.err);
   return cudaGetLastError();

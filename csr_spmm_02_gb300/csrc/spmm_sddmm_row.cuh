@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads)
       // plain store: a group writes 64 bytes of a 128-byte line per round, and
       // both halves must meet in L2 (an evict-first store let half-written
       // lines reach DRAM, about 17x the output's bytes)
-      if (lane < cnt) out[base + lane] = x;
+      if (lane < cnt) st_plain1(out + base + lane, x);
     }
     if (start == end) pc = nstart + lane < nend ? ld_stream(colind + nstart + lane, stream_pol) : 0;
     start = nstart;
@@ -137,6 +137,8 @@ cudaError_t launch_sddmm_row_t(const Launch& L, const float* Cd, float* out) {
   if (e != cudaSuccess) return e;
   const int64_t need = (int64_t(L.M) + kGroups - 1) / kGroups;
   const unsigned grid = unsigned(std::min<int64_t>(need, sddmm_row_blocks<G>(dev)));
+  SPMM_DEBUG_RANGES(L.stream, L.err, {{L.B, size_t(L.K) * L.N * 4}, {Cd, size_t(L.M) * L.N * 4}},
+                    {{out, size_t(L.nnz) * 4}});
   spmm_sddmm_row_kernel<G><<<grid, kThreads, 0, L.stream>>>(L.M, L.N, L.rowptr, L.colind, Cd,
                                                             static_cast<const float*>(L.B), out);
   return cudaGetLastError();
@@ -261,6 +263,9 @@ cudaError_t launch_fusedmm_row_t(const Launch& L, const float* Cd, const float* 
   if (e != cudaSuccess) return e;
   const int64_t need = (int64_t(L.M) + kGroups - 1) / kGroups;
   const unsigned grid = unsigned(std::min<int64_t>(need, fusedmm_row_blocks<G>(dev)));
+  SPMM_DEBUG_RANGES(L.stream, L.err,
+                    {{L.B, size_t(L.K) * L.N * 4}, {Cd, size_t(L.M) * L.N * 4}, {Bd, size_t(L.K) * L.N * 4}},
+                    {{L.C, size_t(L.M) * L.N * 4}});
   spmm_fusedmm_row_kernel<G><<<grid, kThreads, 0, L.stream>>>(L.M, L.N, L.rowptr, L.colind, Cd, Bd,
                                                               static_cast<const float*>(L.B), L.C);
   return cudaGetLastError();

@@ -690,6 +690,7 @@ inline cudaError_t launch_tc_window(const Launch& L) {
   while (cols < uint32_t(L.N)) cols <<= 1;
   const int64_t tiles = (int64_t(L.M) + tc::kRows - 1) / tc::kRows;
   const unsigned grid = unsigned(std::min<int64_t>(tiles, sm_count[dev]));
+  SPMM_DEBUG_RANGES(L.stream, L.err, {{L.B, size_t(L.K) * L.N * 2}}, {{L.C, size_t(L.M) * L.N * 4}});
   spmm_tc_window_kernel<<<grid, tc::kCtaThreads, tc::smem_bytes(L.N), L.stream>>>(
       L.M, L.N, L.K, L.rowptr, L.colind, L.vals, static_cast<const uint16_t*>(L.B), L.C, L.err, cols, map);
   return cudaGetLastError();

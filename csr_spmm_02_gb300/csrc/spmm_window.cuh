@@ -68,6 +68,9 @@ struct WindowGeometry {
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+#ifdef SPMM_DEBUG_BOUNDS
+  if (!debug_load_ok(src, 16)) return;
+#endif
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
@@ -291,6 +294,7 @@ cudaError_t launch_window_t(const Launch& L) {
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
   const dim3 grid(unsigned((int64_t(L.M) + Geo::R - 1) / Geo::R), unsigned((L.N + TW - 1) / TW));
+  SPMM_DEBUG_RANGES(L.stream, L.err, {{L.B, size_t(L.K) * L.N * sizeof(BT)}}, {{L.C, size_t(L.M) * L.N * 4}});
   spmm_window_kernel<BT, VEC><<<grid, kThreads, smem, L.stream>>>(
       L.M, L.N, L.rowptr, L.colind, L.vals, static_cast<const BT*>(L.B), L.C, L.err);
   return cudaGetLastError();

@@ -30,7 +30,7 @@ from . import build as _build
 SPMM_OK = 0
 STATUS_NAMES = {0: "SPMM_OK", 1: "SPMM_ERR_INVALID_ARG", 2: "SPMM_ERR_INVALID_CSR",
                 3: "SPMM_ERR_UNSUPPORTED", 4: "SPMM_ERR_PLAN_MISMATCH", 5: "SPMM_ERR_CUDA",
-                6: "SPMM_ERR_DEVICE_TIMEOUT"}
+                6: "SPMM_ERR_DEVICE_TIMEOUT", 7: "SPMM_ERR_OUT_OF_BOUNDS"}
 KERNELS = {"auto": 0, "row": 1, "balanced": 2, "window": 3, "smalln": 4, "window_tc": 5}
 KERNEL_NAMES = {1: "row", 2: "balanced", 3: "window", 4: "smalln", 5: "window_tc"}
 

@@ -32,6 +32,11 @@
  *
  * Sizes
  *   M, K, N >= 0; 0 <= nnz <= 2^31 - 1.  M = 0 or N = 0 is a successful no-op.
+ *   The nnz-balanced SpMM kernel (SPMM_KERNEL_BALANCED, the semirings and
+ *   spmm_csr_f32_noalloc) addresses B with 32-bit offsets of 16-byte vectors
+ *   (of single elements on the scalar path): it returns SPMM_ERR_UNSUPPORTED
+ *   when K * N / 4 (fp32 B), K * N / 8 (bf16 B) or, on the scalar path, K * N
+ *   exceeds 2^32 - 1.
  *   Any N >= 1 is supported.  16-byte vector paths are used when N is a
  *   multiple of 4 (fp32 B) or 8 (bf16 B) and B and C are 16-byte aligned;
  *   otherwise a scalar path runs with the same results.
@@ -85,7 +90,9 @@ typedef enum {
   SPMM_ERR_UNSUPPORTED = 3,    /* a size the library cannot handle (e.g. nnz >= 2^31) */
   SPMM_ERR_PLAN_MISMATCH = 4,  /* exec called with a plan made for another shape */
   SPMM_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
-  SPMM_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait expired (see above) */
+  SPMM_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait expired (see above) */
+  SPMM_ERR_OUT_OF_BOUNDS = 7   /* only in a bounds-checked build: an index pointed outside
+                                * its buffer and the access was skipped */
 } spmm_status;
 
 /* Kernel family a plan uses. */
@@ -141,15 +148,19 @@ typedef struct {
 
 /*
  * Build a plan for A's row structure (nnz-balanced row partitioning).
- * Reads rowptr (device, M+1 entries) on `stream`: one small kernel computes
- * the row-length statistics and reads rowptr[M], which are copied to the
- * host (this call synchronises `stream` once); a second kernel computes the
- * merge-path partition (a binary search per range over the merged sequence
- * of row ends and nonzeros -- the even nnz split the Sgap page's related
- * work attributes to Yang et al., and the element-balanced EB scheme of its
- * DA-SpMM design space).  nnz must equal rowptr[M]: SPMM_ERR_INVALID_CSR
- * otherwise.  The plan's workspace is allocated with cudaMalloc.  *plan_out
- * receives the plan (NULL on error).
+ * Reads rowptr (device, M+1 entries) on `stream` in one pass (one kernel):
+ * the row-length statistics and rowptr[M], which are copied to the host
+ * (this call synchronises `stream` once), and the merge-path partition -- the
+ * merged sequence of row ends and nonzeros cut into equal ranges, the even
+ * nnz split the Sgap page's related work attributes to Yang et al. and the
+ * element-balanced EB scheme of its DA-SpMM design space; row i's end sits at
+ * position rowptr[i+1] + i, so each row writes the range starts that fall in
+ * it, with no search.  nnz must equal rowptr[M]: SPMM_ERR_INVALID_CSR
+ * otherwise.  The plan's workspace comes stream-ordered on `stream`
+ * (cudaMallocFromPoolAsync) from a pool the library creates on each device
+ * at its first plan; the pool keeps freed blocks reserved for later plans
+ * (spmm_pool_release hands them back).  *plan_out receives the plan (NULL on
+ * error).
  */
 SPMM_API spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
                           void* stream, spmm_plan_t* plan_out);
@@ -183,7 +194,8 @@ SPMM_API spmm_status spmm_plan_set_column_tile(spmm_plan_t plan, int32_t columns
  * the merge-path partition used by the balanced SpMM, SDDMM and FusedMM. */
 SPMM_API spmm_status spmm_plan_get_info(spmm_plan_t plan, spmm_plan_info* info);
 
-/* Free the plan and its workspace (synchronous). NULL is accepted. */
+/* Free the plan and its workspace (synchronises the device first, since the
+ * plan may be in use on any stream).  NULL is accepted. */
 SPMM_API spmm_status spmm_plan_destroy(spmm_plan_t plan);
 
 /*
@@ -257,10 +269,9 @@ SPMM_API spmm_status spmm_csr_fusedmm_f32(spmm_plan_t plan, int32_t K, const int
  * One-call form: plans, multiplies and frees on `stream`.  nnz is read from
  * rowptr[M] with the plan's statistics (one copy, which synchronises `stream`
  * once; SPMM_ERR_INVALID_CSR if it is negative).  The plan's workspace comes
- * stream-ordered (cudaMallocFromPoolAsync / cudaFreeAsync) from a pool the
- * library creates on each device at its first one-call use; the pool keeps
- * freed blocks reserved for later calls (spmm_pool_release hands them back),
- * so repeated calls map no new memory.  The merge-path partition is built
+ * from the library's pool (see spmm_csr_plan) and is returned to it
+ * stream-ordered (cudaFreeAsync) at the end of the call, so repeated calls
+ * map no new memory.  The merge-path partition is built
  * only when the chosen kernel is the balanced one.  For repeated products
  * with the same A, build a plan once and call the _exec form.  A bounded
  * wait that gives up in this call's kernels is recorded in the device's
@@ -288,8 +299,11 @@ SPMM_API spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* col
 
 /*
  * Synchronise `stream`, read and clear the plan's device error word.
- * Returns SPMM_ERR_DEVICE_TIMEOUT if a kernel run with this plan gave up a
- * bounded wait since the last check, else SPMM_OK.
+ * Returns SPMM_ERR_OUT_OF_BOUNDS if (in a library built with
+ * -DSPMM_DEBUG_BOUNDS, where every B-row gather and every output store checks
+ * its address) an access fell outside its buffer, else
+ * SPMM_ERR_DEVICE_TIMEOUT if a kernel run with this plan gave up a bounded
+ * wait since the last check, else SPMM_OK.
  */
 SPMM_API spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream);
 
@@ -352,8 +366,10 @@ SPMM_API spmm_status spmm_csr_row_blocks(const int32_t* rowptr, int32_t M, int32
  * current device.  The word collects the bits of every such call on the
  * device since the last check, whatever its stream.  Returns
  * SPMM_ERR_INVALID_CSR if a spmm_csr_f32_noalloc call was given an nnz other
- * than rowptr[M] (that call wrote nothing), else SPMM_ERR_DEVICE_TIMEOUT if a
- * kernel gave up a bounded wait (its output is incomplete), else SPMM_OK.
+ * than rowptr[M] (that call wrote nothing), else SPMM_ERR_OUT_OF_BOUNDS (a
+ * bounds-checked build only, see spmm_plan_check_device), else
+ * SPMM_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait (its output is
+ * incomplete), else SPMM_OK.
  * Allocates nothing.
  */
 SPMM_API spmm_status spmm_check_device(void* stream);
@@ -368,10 +384,10 @@ SPMM_API spmm_status spmm_check_device(void* stream);
 SPMM_API spmm_status spmm_plan_set_split_event(spmm_plan_t plan, void* event);
 
 /*
- * Return to the system the device memory that the one-call forms' pools
- * (one per device, see spmm_csr_f32) keep reserved between calls.  Blocks
- * still in use, or freed on a stream that has not reached the free yet, stay
- * with the pool: synchronise the streams that ran one-call forms first.
+ * Return to the system the device memory that the library's pools (one per
+ * device, see spmm_csr_plan) keep reserved between plans.  Blocks still in
+ * use (live plans), or freed on a stream that has not reached the free yet,
+ * stay with the pool: synchronise the streams that ran one-call forms first.
  * Safe to call at any time, from any thread; SPMM_ERR_CUDA if a trim fails.
  */
 SPMM_API spmm_status spmm_pool_release(void);
