@@ -454,9 +454,11 @@ def gpu_arm(args, p, cfg, ws, rank, local):
         def step(t=d, o=out):
             spmm.spmm_csr_sddmm_f32(plan, p.K, t["colind"], t["C"], t["B"], o)
     else:
-        # row-class plans with N <= 128 run the group-per-row FusedMM (no fixup launch)
+        # window-class plans run the window FusedMM (N a multiple of 4 up to 512) and other
+        # row-class plans with N <= 128 the group-per-row form: one launch, no fixup
+        window_form = info["kernel"] in ("window", "window_tc") and p.N % 4 == 0 and p.N <= 512
         row_form = info["kernel"] in ("row", "window", "smalln", "window_tc") and p.N <= 128
-        kernel, launches_per_step = "fusedmm", 1 if row_form else 2
+        kernel, launches_per_step = "fusedmm", 1 if (window_form or row_form) else 2
 
         def step(t=d, o=out):
             spmm.spmm_csr_fusedmm_f32(plan, p.K, t["colind"], t["C"], t["B"], t["D"], o)

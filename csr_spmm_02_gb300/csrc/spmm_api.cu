@@ -143,6 +143,10 @@ spmm_status sddmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const floa
   L.K = K;
   L.colind = colind;
   L.B = B;
+  // Window-class plans (rows whose columns are local): the dense window of
+  // each 32-row block from shared memory.
+  const bool window_family = plan->kernel == SPMM_KERNEL_WINDOW || plan->kernel == SPMM_KERNEL_WINDOW_TC;
+  if (window_family && vector_ok && plan->N <= 512) return status_of(launch_window_sddmm_f32(L, Cd, out));
   // Short, even rows (a row-class plan) and one 128-column tile: a group per
   // row keeps the C row in registers.
   const bool row_family = plan->kernel == SPMM_KERNEL_ROW || plan->kernel == SPMM_KERNEL_WINDOW ||
@@ -203,6 +207,14 @@ spmm_status fusedmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const fl
   L.colind = colind;
   L.B = D;  // gathered and accumulated
   L.C = E;
+  // Window-class plans (rows whose columns are local): the dense window of
+  // each 32-row block from shared memory, for both products.
+  const bool window_family = plan->kernel == SPMM_KERNEL_WINDOW || plan->kernel == SPMM_KERNEL_WINDOW_TC;
+  if (window_family && vector_ok && plan->N <= 512) {
+    cudaError_t e = launch_window_fusedmm_f32(L, Cd, B);
+    if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+    return status_of(e);
+  }
   // Short, even rows (a row-class plan) and one 128-column tile: a group per
   // row keeps the C row and the E row in registers.
   const bool row_family = plan->kernel == SPMM_KERNEL_ROW || plan->kernel == SPMM_KERNEL_WINDOW ||

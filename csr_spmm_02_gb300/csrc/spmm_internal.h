@@ -115,6 +115,11 @@ cudaError_t launch_sddmm_f32(const Launch& L, Shape s, const float* Cd, float* o
 // SDDMM with one group of G lanes (4, 8, 16, 32) per row: 4 fp32 columns per lane, N <= 4G.
 cudaError_t launch_sddmm_row_f32(const Launch& L, int G, const float* Cd, float* out);
 cudaError_t launch_fusedmm_f32(const Launch& L, Shape s, const float* Cd, const float* Bd);
+// SDDMM / FusedMM on window-class plans: the dense window of each 32-row block
+// from shared memory (blocks whose columns span more than 96 gather instead).
+// N a multiple of 4, at most 512, operands 16-byte aligned.  FusedMM: L.B is D.
+cudaError_t launch_window_sddmm_f32(const Launch& L, const float* Cd, float* out);
+cudaError_t launch_window_fusedmm_f32(const Launch& L, const float* Cd, const float* Bd);
 // FusedMM with one group of G lanes (4, 8, 16, 32) per row: 4 fp32 columns per lane, N <= 4G; L.B is D.
 cudaError_t launch_fusedmm_row_f32(const Launch& L, int G, const float* Cd, const float* Bd);
 // Merge-path coordinates of the P+1 range starts (ranges of T items) into part.

@@ -217,9 +217,12 @@ SPMM_API spmm_status spmm_csr_bf16f32_exec(spmm_plan_t plan, int32_t K, const in
  * out[p] = sum_n C[i][n] * B[colind[p]][n] for every stored position p of
  * row i.  A's values are not used.  C is M x N, B is K x N (fp32, row-major,
  * N the plan's width); out is fp32[nnz] in CSR order.  A plan whose kernel is
- * ROW, WINDOW, WINDOW_TC or SMALLN (short, even rows) with N <= 128, N a
- * multiple of 4 and 16-byte aligned B and C runs one lane group per row with
- * the C row in registers; otherwise the plan's merge-path ranges.
+ * WINDOW or WINDOW_TC (short rows with local columns) with N <= 512, N a
+ * multiple of 4 and 16-byte aligned B and C computes each 32-row block's dense
+ * window from shared memory (a block whose columns span more than 96 gathers
+ * instead); one whose kernel is ROW or SMALLN with N <= 128 and the same
+ * alignment runs one lane group per row with the C row in registers;
+ * otherwise the plan's merge-path ranges.
  * Asynchronous on `stream`; every output written once, so results are
  * deterministic.  Tolerance-wise each value is an fp32 dot product.
  */
@@ -258,9 +261,12 @@ SPMM_API spmm_status spmm_csr_semiring_f32_exec(spmm_plan_t plan, int32_t K, con
  * E[i] = sum over stored j of row i of (C[i] . B[j]) * D[j], the SDDMM values
  * used at once as the sparse values of an SpMM and never stored.  C is M x N,
  * B and D are K x N, E is M x N (fp32, row-major, N the plan's width).  On the
- * plans and widths where SDDMM runs a group per row (above), one lane group
- * per row keeps C[i] and E[i] in registers; otherwise the nnz-balanced kernel
- * and its fixup run.  Deterministic for a given plan.
+ * plans and widths where SDDMM uses the window (above), both products come
+ * from the window in shared memory (the values stay in shared memory, and
+ * absent entries inside the window are multiplied as zeros, as in the window
+ * SpMM kernel); where SDDMM runs a group per row, one lane group per row
+ * keeps C[i] and E[i] in registers; otherwise the nnz-balanced kernel and its
+ * fixup run.  Deterministic for a given plan.
  */
 SPMM_API spmm_status spmm_csr_fusedmm_f32(spmm_plan_t plan, int32_t K, const int32_t* colind, const float* C,
                                           const float* B, const float* D, float* E, void* stream);

@@ -99,6 +99,58 @@ def test_fusedmm_parity(N):
     H.assert_within(got, ref, fused_bound(p, C, B, D), "f32", f"fusedmm N={N}")
 
 
+def band_problem(seed, M, K, below, above, N, integer=False, **kw):
+    """A band (test_window_gpu's builder) with dense operands C (M x N), B and D (K x N)."""
+    from tests.test_window_gpu import banded
+    p = banded(seed, M, K, below, above, N, integer=integer, **kw)
+    rng = np.random.default_rng(seed + 7)
+    if integer:
+        C, D = rng.integers(-2, 3, (M, N)).astype(np.float32), rng.integers(-2, 3, (K, N)).astype(np.float32)
+    else:
+        C, D = rng.uniform(-1, 1, (M, N)).astype(np.float32), rng.uniform(-1, 1, (K, N)).astype(np.float32)
+    return p, C, p.B, D
+
+
+@pytest.mark.parametrize("kernel", ["window", "window_tc"])
+@pytest.mark.parametrize("N", [4, 64, 128, 136, 256, 512])
+def test_window_sddmm_fusedmm(kernel, N):
+    """Window-class plans: the dense window of each 32-row block from shared memory (a band of
+    64 columns spans at most 95 per block), ragged last block, several 128-column passes and a
+    partial one (N = 136)."""
+    p, C, B, D = band_problem(N, 650, 700, 32, 31, N)
+    ref, S = oracle.sddmm_reference(p.rowptr, p.colind, C, B)
+    got = run_sddmm(p, C, B, kernel=kernel)
+    assert np.all(np.abs(got - ref) <= 1e-5 * S + 1e-30), f"window sddmm N={N}"
+    Eref, _ = oracle.fusedmm_reference(p.rowptr, p.colind, C, B, D)
+    H.assert_within(run_fusedmm(p, C, B, D, kernel=kernel), Eref, fused_bound(p, C, B, D), "f32",
+                    f"window fusedmm N={N}")
+
+
+@pytest.mark.parametrize("case", ["wide", "duplicates", "unsorted", "empty", "sparse", "long"])
+def test_window_sddmm_fusedmm_shapes(case):
+    """Blocks that take the gather path (a span over 96 columns, more nonzeros than the staging
+    area), duplicate entries (FusedMM counts each occurrence), unsorted columns, empty rows and
+    blocks; integer data, so every path must be bitwise exact."""
+    kw = {"wide": dict(below=70, above=70), "duplicates": dict(duplicates=True), "unsorted": dict(unsorted=True),
+          "empty": dict(empty_every=5), "sparse": dict(sparse_every=3),
+          "long": dict(long_rows=[(40, 600), (41, 650), (42, 700), (43, 680)])}[case]
+    below, above = kw.pop("below", 32), kw.pop("above", 31)
+    for N in (64, 256):
+        p, C, B, D = band_problem(90 + N, 400, 720, below, above, N, integer=True, **kw)
+        ref, _ = oracle.sddmm_reference(p.rowptr, p.colind, C, B)
+        assert np.array_equal(run_sddmm(p, C, B, kernel="window"), ref), f"{case} sddmm N={N}"
+        Eref, _ = oracle.fusedmm_reference(p.rowptr, p.colind, C, B, D)
+        assert np.array_equal(run_fusedmm(p, C, B, D, kernel="window"), Eref), f"{case} fusedmm N={N}"
+
+
+def test_window_sddmm_fusedmm_deterministic():
+    p, C, B, D = band_problem(3, 500, 520, 32, 31, 256)
+    a = H.device_arrays(p)
+    assert np.array_equal(run_sddmm(p, C, B, arrays=a, kernel="window"), run_sddmm(p, C, B, arrays=a, kernel="window"))
+    assert np.array_equal(run_fusedmm(p, C, B, D, arrays=a, kernel="window"),
+                          run_fusedmm(p, C, B, D, arrays=a, kernel="window"))
+
+
 @pytest.mark.parametrize("N", [8, 64])
 def test_integer_exact(N):
     p, C, B, D = problem(200 + N, N=N, integer=True)
@@ -156,15 +208,15 @@ def test_empty_pattern():
     assert not bool(E.any()) and bool(torch.isfinite(E).all())
 
 
-@pytest.mark.parametrize("name", ["uniform64k", "rmat22"])
+@pytest.mark.parametrize("name", ["uniform64k", "banded", "rmat22"])
 def test_workload_structures(name):
-    """Full-size patterns of two benchmark workloads (N of the workload): every
-    SDDMM value and every FusedMM output element against the oracles."""
+    """Full-size patterns of three benchmark workloads (N of the workload; banded's bf16 B widened
+    exactly to fp32): every SDDMM value and every FusedMM output element against the oracles."""
     p = gen.make_workload(name)
     rng = np.random.default_rng(5)
     C = rng.uniform(-1, 1, (p.M, p.N)).astype(np.float32)
     D = rng.uniform(-1, 1, (p.K, p.N)).astype(np.float32)
-    B = p.B
+    B = p.B if p.b_dtype == "f32" else (p.B.astype(np.uint32) << 16).view(np.float32)
     absD = np.abs(D)
     a = H.device_arrays(p)
     plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, p.N)
