@@ -346,7 +346,8 @@ def reference_arm(args, p, cfg):
             "impl": "reference", "metric": OP_METRIC[args.op], "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(r[2] for r in runs) / len(runs),
             "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "scaling": "strong" if args.shard == "rows" else "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": "each step: " + runs[-1][1]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -377,7 +378,8 @@ def reference_arm(args, p, cfg):
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+        "scaling": "strong" if args.shard == "rows" else "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": cfg,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -618,15 +620,11 @@ def gpu_arm(args, p, cfg, ws, rank, local):
             cpu_par = {"value": pval, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": pdesc}
 
     cfg = dict(cfg)
-    cfg.update({"op": op, "kernel": kernel, "items_per_cta": info["items_per_cta"], "num_ctas": info["num_ctas"],
+    cfg["l2"] = f"flushed before every timed step (write of {FLUSH_BYTES >> 20} MiB)"
+    plan_rec = {"kernel": kernel, "items_per_cta": info["items_per_cta"], "num_ctas": info["num_ctas"],
                 "plan_ms": round(plan_ms, 3), "plan_first_ms": round(plan_first_ms, 3),
                 "max_row_nnz": info["max_row_nnz"],
-                "l2": f"flushed before every timed step (write of {FLUSH_BYTES >> 20} MiB)",
-                "timing": "CUDA events per step on the launch stream; plan built once before timing"})
-    if op != "spmm":
-        cfg["b_dtype"] = "f32"
-        cfg["compulsory_bytes"] = nbytes
-        cfg["dense_operands"] = "C, D seeded uniform(-1, 1) fp32; B the workload's B in fp32"
+                "timing": "CUDA events per step on the launch stream; plan built once before timing"}
     line = {
         "metric": OP_METRIC[op], "value": value_flops / 1e9, "unit": UNIT, "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -643,7 +641,7 @@ def gpu_arm(args, p, cfg, ws, rank, local):
                      "traffic": traffic, "algorithmic_bytes": nbytes, "kernel_ms": mean_main},
         "gather": gather,
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_par, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": steps * launches_per_step,
+        "gpu_launches": steps * launches_per_step, "plan": plan_rec,
     }
     plan.destroy()
     return line
@@ -687,8 +685,12 @@ def main(argv=None):
         name += f", B redrawn with N={args.n}"
     if args.semiring != ("sum", "mul"):
         name += f", semiring ({args.semiring[0]}, {args.semiring[1]})"
-    cfg = {"workload": name, "M": p.M, "K": p.K, "N": p.N, "nnz": p.nnz, "b_dtype": p.b_dtype,
-           "seed": p.seed, "compulsory_bytes": op_bytes(p, args.op)}
+    cfg = {"workload": name, "M": p.M, "K": p.K, "N": p.N, "nnz": p.nnz,
+           "b_dtype": p.b_dtype if args.op == "spmm" else "f32", "seed": p.seed,
+           "compulsory_bytes": op_bytes(p, args.op), "op": args.op}
+    if args.op != "spmm":
+        cfg["dense_operands"] = "C, D seeded uniform(-1, 1) fp32; B the workload's B in fp32"
+
     if args.impl == "reference":
         print(json.dumps(reference_arm(args, p, cfg)), flush=True)
         return 0
