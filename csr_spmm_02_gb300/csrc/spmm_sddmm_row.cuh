@@ -107,7 +107,14 @@ __global__ void __launch_bounds__(kThreads)
       // plain store: a group writes 64 bytes of a 128-byte line per round, and
       // both halves must meet in L2 (an evict-first store let half-written
       // lines reach DRAM, about 17x the output's bytes)
+#ifdef SPMM_DEBUG_BOUNDS
       if (lane < cnt) st_plain1(out + base + lane, x);
+#else
+      // written out rather than through st_plain1: with the helper the
+      // compiler schedules this loop differently and uniform64k (N = 64)
+      // takes 48 instead of 40 us
+      if (lane < cnt) out[base + lane] = x;
+#endif
     }
     if (start == end) pc = nstart + lane < nend ? ld_stream(colind + nstart + lane, stream_pol) : 0;
     start = nstart;
