@@ -541,7 +541,7 @@ def gpu_arm(args, p, cfg, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         h = {k: torch.from_numpy(v).pin_memory() for k, v in host.items()}
-        if op == "spmm":
+        if op == "spmm" and args.semiring == ("sum", "mul"):
             h["rowptr"] = torch.from_numpy(p.rowptr).pin_memory()
             one_call = spmm.spmm_csr_bf16f32 if bf16 else spmm.spmm_csr_f32
             api = "spmm_csr_bf16f32" if bf16 else "spmm_csr_f32"
@@ -549,7 +549,8 @@ def gpu_arm(args, p, cfg, ws, rank, local):
             def call(t, o, s):
                 one_call(p.M, p.K, p.N, t["rowptr"], t["colind"], t["vals"], t["B"], o, stream=s)
         else:
-            api = (f"spmm_csr_{op}_f32 on a plan built once for the fixed pattern "
+            fn = "semiring_f32_exec" if op == "spmm" else f"{op}_f32"
+            api = (f"spmm_csr_{fn} on a plan built once for the fixed pattern "
                    "(rowptr is not re-sent; colind and the dense operands are)")
 
             def call(t, o, s):

@@ -47,7 +47,8 @@ struct spmm_plan_s {
   float* carry = nullptr; // [num_ctas][2][N] partial rows split across CTAs
   int* err = nullptr;     // device error word (the plan's own, or the one-call forms' shared word)
   int* stats = nullptr;   // [3]: max row length, empty rows, rowptr[M]
-  void* small = nullptr;  // the 16-byte allocation holding the plan's own error word and stats
+  void* small = nullptr;  // one-call forms: the 16-byte allocation holding the error word and stats
+                         // (a plan keeps them in the first 256 bytes of its workspace)
   cudaEvent_t split_event = nullptr;  // recorded between main kernel and fixup
 };
 

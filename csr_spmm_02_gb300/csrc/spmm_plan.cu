@@ -32,10 +32,18 @@ __global__ void __launch_bounds__(kThreads) plan_rows_kernel(const int32_t* __re
     longest = max(longest, len);
     empty += len == 0;
     if (part) {
-      const int64_t prev_end = int64_t(a) + i - 1;  // e(i-1); -1 for the first row
-      const int64_t c0 = prev_end < 0 ? 0 : prev_end / T + 1;
-      const int64_t c1 = min((int64_t(b) + i) / T, int64_t(P) - 1);
-      for (int64_t c = c0; c <= c1; ++c) part[c] = make_int2(int(i), int(c * T - i));
+      // Row i's items end at e(i) = b + i, below 2^32 since nnz and M are
+      // each below 2^31: 32-bit arithmetic.  The diagonals that start inside
+      // row i are the multiples of T in (e(i-1), e(i)] = (e - len - 1, e];
+      // with q = e / T and r = e - q*T there are none unless r <= len.
+      const uint32_t e = uint32_t(b) + uint32_t(i), ut = uint32_t(T);
+      const uint32_t q = e / ut, r = e - q * ut;
+      if (r <= uint32_t(len)) {
+        const uint32_t s = uint32_t(a) + uint32_t(i);  // e(i-1) + 1
+        const uint32_t first = s == 0 ? 0u : (s - 1u) / ut + 1u;
+        const uint32_t last = min(q, uint32_t(P) - 1u);
+        for (uint32_t c = first; c <= last; ++c) part[c] = make_int2(int(i), int(c * ut - uint32_t(i)));
+      }
     }
   }
 #pragma unroll
@@ -211,6 +219,19 @@ void dev_free(void* p, cudaStream_t s) {
   if (p) cudaFreeAsync(p, s);
 }
 
+// A pinned host buffer per host thread for the plan's one read-back of its
+// statistics (an asynchronous copy into it needs no staging through a driver
+// buffer, unlike one into pageable memory).  Allocated on the thread's first
+// plan and kept for the life of the process.
+int* pinned_stats_buffer() {
+  thread_local int* buf = nullptr;
+  if (!buf) {
+    void* p = nullptr;
+    if (cudaHostAlloc(&p, 16, cudaHostAllocPortable) == cudaSuccess) buf = static_cast<int*>(p);
+  }
+  return buf;
+}
+
 unsigned stats_grid(int32_t M) {
   const int64_t blocks = (int64_t(M) + kThreads - 1) / kThreads;
   return unsigned(std::max<int64_t>(1, std::min<int64_t>(blocks, 152 * 8)));
@@ -262,38 +283,46 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   // forms learn nnz from that pass and build the partition afterwards, only
   // when the balanced kernel is chosen.
   const int T = items_per_cta ? items_per_cta : default_items_per_cta(N);
-  auto carve = [&](int64_t P) -> spmm_status {  // partition + carry rows for P ranges
+  auto carve = [&](int64_t P, size_t head) -> spmm_status {  // [head] + partition + carry rows for P ranges
     if (P > INT32_MAX - 1) return SPMM_ERR_UNSUPPORTED;
     plan->items_per_cta = T;
     plan->num_ctas = int32_t(P);
     const size_t part_bytes = (size_t(P) + 1) * sizeof(int2);
     const size_t part_padded = (part_bytes + 255) & ~size_t(255);
     const size_t carry_bytes = size_t(P) * 2 * size_t(N) * sizeof(float);
-    plan->workspace_bytes = int64_t(part_padded + carry_bytes);
-    if (dev_alloc(&plan->workspace, part_padded + carry_bytes, stream) != cudaSuccess) return SPMM_ERR_CUDA;
-    plan->part = static_cast<int2*>(plan->workspace);
-    plan->carry = reinterpret_cast<float*>(static_cast<char*>(plan->workspace) + part_padded);
+    plan->workspace_bytes += int64_t(head + part_padded + carry_bytes);
+    if (dev_alloc(&plan->workspace, head + part_padded + carry_bytes, stream) != cudaSuccess) return SPMM_ERR_CUDA;
+    char* w = static_cast<char*>(plan->workspace);
+    plan->part = reinterpret_cast<int2*>(w + head);
+    plan->carry = reinterpret_cast<float*>(w + head + part_padded);
     return SPMM_OK;
   };
   const int64_t P_known = one_call ? 0 : (int64_t(M) + nnz + T - 1) / T;
+  // The error word and statistics (16 bytes): the head of the workspace in
+  // the plan form (one allocation), an allocation of their own in the
+  // one-call forms, whose workspace size is known only after the statistics.
   if (!one_call) {
-    const spmm_status st = carve(P_known);
+    const spmm_status st = carve(P_known, 256);
     if (st != SPMM_OK) return fail(st);
+    plan->err = static_cast<int*>(plan->workspace);
+  } else {
+    if (dev_alloc(&plan->small, 16, stream) != cudaSuccess) return fail(SPMM_ERR_CUDA);
+    plan->workspace_bytes += 16;
+    plan->err = static_cast<int*>(plan->small);
   }
-
-  // error word + statistics (16 bytes)
-  cudaError_t e = dev_alloc(&plan->small, 16, stream);
-  if (e != cudaSuccess) return fail(SPMM_ERR_CUDA);
-  plan->err = static_cast<int*>(plan->small);
   plan->stats = plan->err + 1;
-  if ((e = cudaMemsetAsync(plan->small, 0, 16, stream)) != cudaSuccess) return fail(SPMM_ERR_CUDA);
+  cudaError_t e = cudaMemsetAsync(plan->err, 0, 16, stream);
+  if (e != cudaSuccess) return fail(SPMM_ERR_CUDA);
   plan_rows_kernel<<<stats_grid(M), kThreads, 0, stream>>>(rowptr, M, std::max<int64_t>(nnz, 0), T, int32_t(P_known),
                                                            plan->stats, plan->part);
   if ((e = cudaGetLastError()) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   int host_stats[3] = {0, 0, 0};
-  if ((e = cudaMemcpyAsync(host_stats, plan->stats, sizeof host_stats, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+  int* pinned = pinned_stats_buffer();
+  if ((e = cudaMemcpyAsync(pinned ? pinned : host_stats, plan->stats, sizeof host_stats, cudaMemcpyDeviceToHost,
+                           stream)) != cudaSuccess)
     return fail(SPMM_ERR_CUDA);
   if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return fail(SPMM_ERR_CUDA);
+  if (pinned) std::copy(pinned, pinned + 3, host_stats);
   plan->max_row_nnz = host_stats[0];
   plan->empty_rows = host_stats[1];
   if (host_stats[2] < 0 || (nnz >= 0 && host_stats[2] != nnz)) return fail(SPMM_ERR_INVALID_CSR);
@@ -325,12 +354,11 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   // balanced kernel (a one-call SpMM on another kernel needs neither)
   if (one_call && plan->kernel == SPMM_KERNEL_BALANCED) {
     const int64_t P = (int64_t(M) + nnz + T - 1) / T;
-    const spmm_status st = carve(P);
+    const spmm_status st = carve(P, 0);
     if (st != SPMM_OK) return fail(st);
     plan_rows_kernel<<<stats_grid(M), kThreads, 0, stream>>>(rowptr, M, nnz, T, int32_t(P), plan->stats, plan->part);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(SPMM_ERR_CUDA);
   }
-  plan->workspace_bytes += 16;
   *plan_out = plan;
   return SPMM_OK;
 }
