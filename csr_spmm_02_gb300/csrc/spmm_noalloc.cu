@@ -67,7 +67,7 @@ extern "C" SPMM_API spmm_status spmm_csr_f32_noalloc(int32_t M, int32_t K, int32
                                                      const float* vals, const float* B, float* C, void* stream) {
   using namespace spmm;
   if (M < 0 || K < 0 || N < 0 || nnz < 0) return SPMM_ERR_INVALID_ARG;
-  if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+  if (M > SPMM_MAX_EXTENT || nnz > SPMM_MAX_EXTENT) return SPMM_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return SPMM_OK;
   if (!rowptr || !C || (nnz > 0 && (!colind || !vals || !B || K == 0))) return SPMM_ERR_INVALID_ARG;
 

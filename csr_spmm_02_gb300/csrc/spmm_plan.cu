@@ -248,7 +248,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   if (!plan_out) return SPMM_ERR_INVALID_ARG;
   *plan_out = nullptr;
   if (M < 0 || N < 0 || (nnz < 0 && !one_call)) return SPMM_ERR_INVALID_ARG;
-  if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+  if (M > SPMM_MAX_EXTENT || nnz > SPMM_MAX_EXTENT) return SPMM_ERR_UNSUPPORTED;
   if (M > 0 && !rowptr) return SPMM_ERR_INVALID_ARG;
   if (kernel < SPMM_KERNEL_AUTO || kernel > SPMM_KERNEL_WINDOW_TC) return SPMM_ERR_INVALID_ARG;
   if (items_per_cta != 0 && (items_per_cta < 256 || items_per_cta > kMaxItemsPerCta || items_per_cta % 256 != 0))
@@ -326,6 +326,7 @@ spmm_status spmm_make_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_
   plan->max_row_nnz = host_stats[0];
   plan->empty_rows = host_stats[1];
   if (host_stats[2] < 0 || (nnz >= 0 && host_stats[2] != nnz)) return fail(SPMM_ERR_INVALID_CSR);
+  if (host_stats[2] > SPMM_MAX_EXTENT) return fail(SPMM_ERR_UNSUPPORTED);  // one-call forms: nnz from rowptr[M]
   nnz = plan->nnz = host_stats[2];
 
   if (kernel == SPMM_KERNEL_AUTO) {
@@ -436,7 +437,7 @@ spmm_status spmm_plan_check_device(spmm_plan_t plan, void* stream) {
 spmm_status spmm_csr_validate(const int32_t* rowptr, const int32_t* colind, int32_t M, int32_t K, int64_t nnz,
                               void* stream) {
   if (M < 0 || K < 0 || nnz < 0) return SPMM_ERR_INVALID_ARG;
-  if (nnz > INT32_MAX) return SPMM_ERR_UNSUPPORTED;
+  if (M > SPMM_MAX_EXTENT || nnz > SPMM_MAX_EXTENT) return SPMM_ERR_UNSUPPORTED;
   if (!rowptr || (nnz > 0 && !colind)) return SPMM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* flag = nullptr;

@@ -31,7 +31,10 @@
  *   stream).  All calls are asynchronous on `stream` unless stated.
  *
  * Sizes
- *   M, K, N >= 0; 0 <= nnz <= 2^31 - 1.  M = 0 or N = 0 is a successful no-op.
+ *   M, K, N >= 0; M <= SPMM_MAX_EXTENT and 0 <= nnz <= SPMM_MAX_EXTENT
+ *   (2^31 - 65536: the kernels index rows and nonzeros in 32 bits and step
+ *   past the last one by small offsets, which must not overflow); larger M
+ *   or nnz return SPMM_ERR_UNSUPPORTED.  M = 0 or N = 0 is a successful no-op.
  *   The nnz-balanced SpMM kernel (SPMM_KERNEL_BALANCED, the semirings and
  *   spmm_csr_f32_noalloc) addresses B with 32-bit offsets of 16-byte vectors
  *   (of single elements on the scalar path): it returns SPMM_ERR_UNSUPPORTED
@@ -71,6 +74,9 @@
 
 #include <stdint.h>
 
+/* Largest M and nnz the library accepts (2^31 - 65536). */
+#define SPMM_MAX_EXTENT 2147418112
+
 /* Only the functions below are exported; everything else in the library is
  * hidden (it is built with -fvisibility=hidden). */
 #if defined(__GNUC__)
@@ -87,7 +93,7 @@ typedef enum {
   SPMM_OK = 0,
   SPMM_ERR_INVALID_ARG = 1,    /* bad size, NULL pointer, unknown option */
   SPMM_ERR_INVALID_CSR = 2,    /* spmm_csr_validate found a malformed CSR */
-  SPMM_ERR_UNSUPPORTED = 3,    /* a size the library cannot handle (e.g. nnz >= 2^31) */
+  SPMM_ERR_UNSUPPORTED = 3,    /* a size the library cannot handle (e.g. nnz > SPMM_MAX_EXTENT) */
   SPMM_ERR_PLAN_MISMATCH = 4,  /* exec called with a plan made for another shape */
   SPMM_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
   SPMM_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait expired (see above) */

@@ -49,8 +49,17 @@ def test_argument_errors_without_cuda(lib):
     assert lib.spmm_csr_plan(null, 4, 0, 4, null, ctypes.byref(out)) == 1  # NULL rowptr with M > 0
     assert lib.spmm_csr_plan_ex(ctypes.c_void_p(16), 4, 0, 4, 7, 0, null, ctypes.byref(out)) == 1
     assert lib.spmm_csr_plan_ex(ctypes.c_void_p(16), 4, 0, 4, 0, 300, null, ctypes.byref(out)) == 1
-    # nnz beyond int32: UNSUPPORTED
+    # M or nnz beyond SPMM_MAX_EXTENT (2^31 - 65536): UNSUPPORTED, at every entry point
+    big = (1 << 31) - 65536 + 1
     assert lib.spmm_csr_plan(ctypes.c_void_p(16), 4, 1 << 31, 4, null, ctypes.byref(out)) == 3
+    assert lib.spmm_csr_plan(ctypes.c_void_p(16), 4, big, 4, null, ctypes.byref(out)) == 3
+    assert lib.spmm_csr_plan(ctypes.c_void_p(16), big, 4, 4, null, ctypes.byref(out)) == 3
+    assert lib.spmm_csr_f32_noalloc(4, 4, 4, big, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                    ctypes.c_void_p(16), ctypes.c_void_p(16), null) == 3
+    assert lib.spmm_csr_f32_noalloc(big, 4, 4, 4, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                    ctypes.c_void_p(16), ctypes.c_void_p(16), null) == 3
+    assert lib.spmm_csr_validate(ctypes.c_void_p(16), ctypes.c_void_p(16), big, 4, 4, null) == 3
+    assert lib.spmm_csr_validate(ctypes.c_void_p(16), ctypes.c_void_p(16), 4, 4, big, null) == 3
     # exec without a plan: PLAN_MISMATCH
     assert lib.spmm_csr_f32_exec(null, 4, null, null, null, null, null) == 4
     assert lib.spmm_csr_bf16f32_exec(null, 4, null, null, null, null, null) == 4
@@ -119,6 +128,11 @@ int main(void) {
   return bad;
 }
 """
+
+
+def test_header_states_the_size_limit():
+    m = re.search(r"#define SPMM_MAX_EXTENT (\d+)", open(HEADER).read())
+    assert m and int(m.group(1)) == (1 << 31) - 65536
 
 
 def test_header_is_c99_and_a_c_program_links(lib, tmp_path):
