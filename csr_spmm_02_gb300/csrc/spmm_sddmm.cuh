@@ -14,7 +14,8 @@
 //  * a warp takes rounds of 32 consecutive nonzeros; its S = 32/G lane groups
 //    take every S-th one, each lane holding VEC*NCH columns of both operands
 //    (16-byte loads; the C row is re-read per nonzero and is an L1 hit while
-//    the row lasts, so no load waits on a row change);
+//    the row lasts, so no load waits on a row change; a round that lies in
+//    one row loads it once);
 //  * a lane keeps the partial dot products of G nonzeros and the group sums
 //    them with a transposed butterfly: G-1 shuffles for G results instead of
 //    log2(G) per result, after which lane l of the group holds nonzero l's
@@ -149,6 +150,59 @@ __device__ __forceinline__ float group_reduce_transposed(float (&v)[P], int gl) 
   return v[0];
 }
 
+// The dot products of one round of R steps (S = 32/G nonzeros each) starting
+// at nonzero base.  ONE_ROW: all of the round's nonzeros lie in one row (long
+// rows), so each lane loads its C slice once for the round instead of once per
+// nonzero.
+template <int VEC, int G, int NCH, int U, int R, bool ONE_ROW>
+__device__ __forceinline__ void sddmm_round_dots(int base, int p1, int nbase, const int* s_col, const int* s_row, int N,
+                                                 const float* __restrict__ B, const float* __restrict__ Crow0,
+                                                 const int (&coffl)[NCH], const bool (&valid)[NCH], int grp, int gl,
+                                                 float (&dots)[R]) {
+  constexpr int S = 32 / G;
+  FVec<VEC> crow[NCH];
+  if constexpr (ONE_ROW) {
+    const size_t coff = size_t(s_row[base - nbase]) * N;
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+      BSlice<float, VEC> x;
+      x.load(Crow0 + coff + coffl[ch]);
+      x.widen(crow[ch]);
+    }
+  }
+#pragma unroll
+  for (int s0 = 0; s0 < R; s0 += U) {
+    BSlice<float, VEC> bs[U][NCH], cs[ONE_ROW ? 1 : U][NCH];
+    int ks[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {  // gathers first: both operand rows of U nonzeros
+      const int k = min(base + (s0 + u) * S + grp, p1 - 1) - nbase;
+      ks[u] = k;
+      const size_t boff = size_t(s_col[k]) * N;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(B + boff + coffl[ch]);
+      if constexpr (!ONE_ROW) {
+        const size_t coff = size_t(s_row[k]) * N;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) cs[u][ch].load(Crow0 + coff + coffl[ch]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      FVec<VEC> b[NCH], c[NCH];
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        bs[u][ch].widen(b[ch]);
+        if constexpr (ONE_ROW) c[ch] = crow[ch]; else cs[u][ch].widen(c[ch]);
+      }
+      float d = dot_lane<VEC, NCH>(c, b, valid);
+      if (N > G * VEC * NCH)
+        d += dot_tail_tiles<VEC, G, NCH>(Crow0 + size_t(s_row[ks[u]]) * N, B + size_t(s_col[ks[u]]) * N, N, gl);
+      dots[s0 + u] = d;
+    }
+  }
+}
+
 template <int VEC, int G, int NCH>
 __global__ void __launch_bounds__(kThreads, SPMM_SDDMM_MIN_BLOCKS)
     spmm_sddmm_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr, const int32_t* __restrict__ colind,
@@ -223,36 +277,19 @@ __global__ void __launch_bounds__(kThreads, SPMM_SDDMM_MIN_BLOCKS)
   const float* Crow0 = Cd + size_t(i0) * N;
   for (int base = p0 + w * NPI; base < p1; base += W * NPI) {
     float dots[R];
-#pragma unroll
-    for (int s0 = 0; s0 < R; s0 += U) {
-      BSlice<float, VEC> bs[U][NCH], cs[U][NCH];
-      int ks[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {  // gathers first: both operand rows of U nonzeros
-        const int k = min(base + (s0 + u) * S + grp, p1 - 1) - nbase;
-        ks[u] = k;
-        const size_t boff = size_t(s_col[k]) * N;
-        const size_t coff = size_t(s_row[k]) * N;
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          bs[u][ch].load(B + boff + coffl[ch]);
-          cs[u][ch].load(Crow0 + coff + coffl[ch]);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        FVec<VEC> b[NCH], c[NCH];
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          bs[u][ch].widen(b[ch]);
-          cs[u][ch].widen(c[ch]);
-        }
-        float d = dot_lane<VEC, NCH>(c, b, valid);
-        if (N > G * VEC * NCH)
-          d += dot_tail_tiles<VEC, G, NCH>(Crow0 + size_t(s_row[ks[u]]) * N, B + size_t(s_col[ks[u]]) * N, N, gl);
-        dots[s0 + u] = d;
-      }
-    }
+    // Rows are non-decreasing along the nonzeros: first == last means one row
+    // (warp-uniform).  Groups of 8 and 16 lanes take the one-row form (rmat22
+    // 1,029 -> 980 us at N = 32, rmat20 554 -> 525 us at N = 64); 32-lane
+    // groups keep one form, as the second one's registers spilled (rmat20
+    // 1,033 -> 1,402 us at N = 128), and 4-lane groups were slower with it
+    // (rmat22 619 -> 670 us at N = 16).
+    constexpr bool kOneRowForm = G >= 8 && G < 32;
+    if (kOneRowForm && s_row[base - nbase] == s_row[min(base + NPI, p1) - 1 - nbase])
+      sddmm_round_dots<VEC, G, NCH, U, R, kOneRowForm>(base, p1, nbase, s_col, s_row, N, B, Crow0, coffl, valid, grp,
+                                                       gl, dots);
+    else
+      sddmm_round_dots<VEC, G, NCH, U, R, false>(base, p1, nbase, s_col, s_row, N, B, Crow0, coffl, valid, grp, gl,
+                                                 dots);
 #pragma unroll
     for (int r0 = 0; r0 < R; r0 += G) {  // one round: G steps, S*G = 32 nonzeros
       float v[G];

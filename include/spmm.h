@@ -166,7 +166,9 @@ typedef struct {
  * (cudaMallocFromPoolAsync) from a pool the library creates on each device
  * at its first plan; the pool keeps freed blocks reserved for later plans
  * (spmm_pool_release hands them back).  *plan_out receives the plan (NULL on
- * error).
+ * error).  A plan's workspace (range carry rows, error word) serves one call
+ * at a time: calls that may overlap on the device (several streams) need a
+ * plan each.
  */
 SPMM_API spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
                           void* stream, spmm_plan_t* plan_out);
