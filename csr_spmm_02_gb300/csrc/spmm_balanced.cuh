@@ -9,7 +9,7 @@
 // and the element-balanced (EB) choice in its DA-SpMM design space, made to
 // count output rows too.  A range starting at diagonal d begins at row
 // r(d) = #{rows whose end lies before d} and nonzero d - r(d); the plan
-// computes these coordinates once per CTA by binary search over rowptr.
+// computes these coordinates once per CTA (spmm_plan.cu).
 //
 // One CTA per range [(i0, p0), (i1, p1)) of T items:
 //  1. stages the range's colind and vals and rowptr[i0..i1] in shared memory
