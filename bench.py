@@ -486,6 +486,17 @@ def gpu_arm(args, p, cfg, ws, rank, local):
     for e in splits:
         e.record()  # create the events before the timed region
     torch.cuda.synchronize()
+    # --graph: every timed step replays one captured step (launch-bound
+    # workloads; the exec calls capture once their kernels have run)
+    run_step = step
+    if args.graph:
+        if split:
+            raise SystemExit("--graph times one-launch steps (this plan's step is a kernel and its fixup)")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        run_step = graph.replay
 
     sampler = ClockSampler(local) if rank == 0 else None
     barrier()
@@ -498,7 +509,7 @@ def gpu_arm(args, p, cfg, ws, rank, local):
         if split:
             spmm.spmm_plan_set_split_event(plan, splits[i])
         starts[i].record(stream)
-        step()
+        run_step()
         ends[i].record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -511,7 +522,7 @@ def gpu_arm(args, p, cfg, ws, rank, local):
     wst = [torch.cuda.Event(enable_timing=True) for _ in range(n_warm + 1)]
     for i in range(n_warm):
         wst[i].record(stream)
-        step()
+        run_step()
     wst[n_warm].record(stream)
     torch.cuda.synchronize()
     warm_ms = [a.elapsed_time(b) for a, b in zip(wst[:-1], wst[1:])]
@@ -635,7 +646,8 @@ def gpu_arm(args, p, cfg, ws, rank, local):
     plan_rec = {"kernel": kernel, "items_per_cta": info["items_per_cta"], "num_ctas": info["num_ctas"],
                 "plan_ms": round(plan_ms, 3), "plan_first_ms": round(plan_first_ms, 3),
                 "max_row_nnz": info["max_row_nnz"],
-                "timing": "CUDA events per step on the launch stream; plan built once before timing"}
+                "timing": "CUDA events per step on the launch stream; plan built once before timing"
+                + ("; each step replayed from a captured CUDA graph" if args.graph else "")}
     line = {
         "metric": OP_METRIC[op], "value": value_flops / 1e9, "unit": UNIT, "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -673,6 +685,7 @@ def main(argv=None):
     ap.add_argument("--semiring", default="sum,mul", help="(+),(x): sum|min|max , mul|add (SpMM only)")
     ap.add_argument("--group-lanes", type=int, default=0, help="lanes per row of a smalln plan")
     ap.add_argument("--column-tile", type=int, default=0, help="N-slicing: cap the column tile (row/balanced)")
+    ap.add_argument("--graph", action="store_true", help="replay each timed step from a captured CUDA graph")
     ap.add_argument("--items-per-cta", type=int, default=0)
     ap.add_argument("--shard", choices=["rows", "replicas"], default="rows",
                     help="under torchrun: split one A into row blocks (rows) or run a replica per rank")

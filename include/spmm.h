@@ -210,6 +210,13 @@ SPMM_API spmm_status spmm_plan_destroy(spmm_plan_t plan);
  * C = A . B with fp32 B, using a plan made for this A (same rowptr, M, nnz,
  * N).  K is B's row count (colind values must lie in [0, K)).  Asynchronous
  * on `stream`.  Returns SPMM_ERR_PLAN_MISMATCH for a NULL plan.
+ *
+ * CUDA graphs: the exec calls (SpMM, SDDMM, FusedMM, semirings) make no
+ * synchronous CUDA call and allocate nothing.  The first call of each
+ * kernel on a device sets that kernel's shared-memory attribute; after it,
+ * an exec call can be captured on `stream` into a CUDA graph, and every
+ * replay reads the captured buffers as they are when it runs.  (Plans and
+ * the one-call forms synchronise and cannot be captured.)
  */
 SPMM_API spmm_status spmm_csr_f32_exec(spmm_plan_t plan, int32_t K, const int32_t* colind,
                               const float* vals, const float* B, float* C, void* stream);
