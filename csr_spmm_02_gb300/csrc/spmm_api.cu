@@ -105,7 +105,12 @@ spmm_status exec(spmm_plan_t plan, int32_t K, const int32_t* colind, const float
     e = bf16 ? launch_row_bf16(L, s) : launch_row_f32(L, s);
     if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
   } else {
-    e = bf16 ? launch_balanced_bf16(L, s) : launch_balanced_f32(L, s);
+    // narrow rows: a whole output row fits one thread, so each thread takes
+    // its own slice of the range (no warp butterfly per row end)
+    if (thread_ranges_shape(plan->N, bf16, vector_ok))
+      e = launch_thread_ranges(L, bf16, vector_ok);
+    else
+      e = bf16 ? launch_balanced_bf16(L, s) : launch_balanced_f32(L, s);
     if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
     if (e == cudaSuccess) e = launch_fixup(L);
   }
