@@ -146,9 +146,17 @@ constexpr int kDefaultItemsPerCta = 2048;
 // 9 to 32 columns put four to eight nonzeros in a warp step, so a range of a
 // given size holds more row ends per step of work; 3072 items per CTA
 // measured best there (R-MAT scale 22, N = 32: SpMM 848 -> 790 us, FusedMM
-// 2.05 -> 1.96 ms), 2048 elsewhere (N = 64 and 128, and the small-N case
-// N = 4, were slower at 3072).
-inline int default_items_per_cta(int32_t N) { return N > 8 && N <= 32 ? 3072 : kDefaultItemsPerCta; }
+// 2.05 -> 1.96 ms).  N = 1 and 4 run the thread-range kernel, whose CTAs
+// amortise their staging, searches and scan over more items at 3840 (15 per
+// thread; the rmat20 pattern at N = 1 119 -> 113 us, N = 4 167 -> 138 us);
+// N = 3 (lane groups) also gained there (165 -> 150 us).  2048 elsewhere:
+// N = 2, whose threads gather in batches of four (136 -> 206 us at 3840),
+// and N = 5 .. 8, 64 and 128.
+inline int default_items_per_cta(int32_t N) {
+  if (N > 8 && N <= 32) return 3072;
+  if (N == 1 || N == 3 || N == 4) return 3840;
+  return kDefaultItemsPerCta;
+}
 
 constexpr int kMaxItemsPerCta = 8192;
 constexpr int kMaxDevices = 64;

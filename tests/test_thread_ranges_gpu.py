@@ -95,3 +95,30 @@ def test_deterministic():
     torch.cuda.synchronize()
     assert all(torch.equal(outs[0], o) for o in outs[1:])
     plan.destroy()
+
+
+@pytest.mark.parametrize("N", [1, 3, 4])
+def test_default_ranges_for_sddmm_and_fusedmm(N):
+    """Plans at N = 1, 3 and 4 take 3840-item ranges by default; the merge-path
+    SDDMM and fused kernels run on the same ranges."""
+    import oracle
+    p = _problem(900 + N, N, "f32", integer=True)
+    a = H.device_arrays(p)
+    plan = spmm.spmm_csr_plan(a["rowptr"], p.M, p.nnz, N, kernel="balanced")
+    assert plan.info()["items_per_cta"] == 3840
+    rng = np.random.default_rng(N)
+    Cd = rng.integers(-2, 3, (p.M, N)).astype(np.float32)
+    Bd = rng.integers(-2, 3, (p.K, N)).astype(np.float32)
+    D = rng.integers(-2, 3, (p.K, N)).astype(np.float32)
+    Cg, Bg, Dg = (torch.from_numpy(x).cuda() for x in (Cd, Bd, D))
+    out = torch.empty(p.nnz, device="cuda")
+    spmm.spmm_csr_sddmm_f32(plan, p.K, a["colind"], Cg, Bg, out)
+    E = torch.empty((p.M, N), device="cuda")
+    spmm.spmm_csr_fusedmm_f32(plan, p.K, a["colind"], Cg, Bg, Dg, E)
+    torch.cuda.synchronize()
+    assert spmm.spmm_plan_check_device(plan) == 0
+    ref, _ = oracle.sddmm_reference(p.rowptr, p.colind, Cd, Bd)
+    assert np.array_equal(out.cpu().numpy().astype(np.float64), ref)
+    Eref, _ = oracle.fusedmm_reference(p.rowptr, p.colind, Cd, Bd, D)
+    assert np.array_equal(E.cpu().numpy().astype(np.float64), Eref)
+    plan.destroy()
