@@ -122,6 +122,19 @@ def test_bounds_build_catches_a_bad_column(flavored, bad):
     spmm.spmm_csr_f32(p.M, p.K, p.N, a["rowptr"], a["colind"], a["vals"], a["B"], C)
     assert spmm.spmm_check_device() == OUT_OF_BOUNDS
     assert spmm.spmm_check_device() == 0
+    # narrow B on a balanced plan: the thread-range kernel (scalar and vector loads)
+    for N in (1, 4):
+        q = gen.random_csr(rng, 700, 400, N, mean_row=8, empty_frac=0.2, long_rows=[(9, 400)])
+        colq = q.colind.copy()
+        colq[[3, len(colq) // 2, len(colq) - 1]] = q.K + 7 if bad == "K+7" else bad
+        b = H.device_arrays(q)
+        b["colind"] = torch.from_numpy(colq).cuda()
+        plan = spmm.spmm_csr_plan(b["rowptr"], q.M, q.nnz, N, kernel="balanced")
+        C = torch.empty((q.M, N), device="cuda")
+        spmm.spmm_csr_f32_exec(plan, q.K, b["colind"], b["vals"], b["B"], C)
+        assert spmm.spmm_plan_check_device(plan) == OUT_OF_BOUNDS, f"thread ranges, N={N}"
+        assert spmm.spmm_plan_check_device(plan) == 0
+        plan.destroy()
 
 
 def test_stage_timeout_is_reported(flavored):
@@ -134,6 +147,15 @@ def test_stage_timeout_is_reported(flavored):
     assert plan.info()["num_ctas"] > 500
     C = torch.empty((p.M, p.N), device="cuda")
     spmm.spmm_csr_f32_exec(plan, p.K, a["colind"], a["vals"], a["B"], C)
+    assert spmm.spmm_plan_check_device(plan) == TIMEOUT
+    assert spmm.spmm_plan_check_device(plan) == 0
+    plan.destroy()
+    # the thread-range kernel (N = 4) takes the same first wait
+    q = gen.random_csr(rng, 20000, 5000, 4, mean_row=12, empty_frac=0.3, long_rows=[(77, 5000)])
+    b = H.device_arrays(q)
+    plan = spmm.spmm_csr_plan(b["rowptr"], q.M, q.nnz, 4, kernel="balanced", items_per_cta=256)
+    C4 = torch.empty((q.M, 4), device="cuda")
+    spmm.spmm_csr_f32_exec(plan, q.K, b["colind"], b["vals"], b["B"], C4)
     assert spmm.spmm_plan_check_device(plan) == TIMEOUT
     assert spmm.spmm_plan_check_device(plan) == 0
     plan.destroy()
