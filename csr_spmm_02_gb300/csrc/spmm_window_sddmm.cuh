@@ -14,11 +14,13 @@
 //  * a CTA takes 32 rows, stages their column indices and finds the span
 //    [cmin, cmax] of columns they touch; if it holds at most 96 columns:
 //  * phase 1, 128 columns of N at a time: the B rows of the window and the
-//    CTA's C rows are copied into shared memory (16-byte cp.async), and each
-//    warp computes the dot products of its 4 rows with all 96 window columns
-//    (lane l owns columns l, l + 32, l + 64: 12 sums, each B slice reused for
-//    4 rows and each C slice for 3 columns, 16-byte shared loads, rows padded
-//    to 132 floats so that those loads are free of bank conflicts);
+//    CTA's C rows are copied into shared memory (16-byte cp.async); warps g
+//    and g + 4 compute the dot products of rows 8g .. 8g+7 with all 96 window
+//    columns over the first and the second half of the pass's columns (lane
+//    l owns columns l, l + 32, l + 64: 24 sums, each B slice reused for 8 rows
+//    and each C slice for 3 columns, 16-byte shared loads, rows padded to 132
+//    floats so that those loads are free of bank conflicts); the halves are
+//    added and each value goes to the tile of the warp that owns its row;
 //  * SDDMM: each stored (i, j) takes its dot product from the warp's tile;
 //    FusedMM: the tile is masked by the pattern (a stored (i, j) counts once
 //    per occurrence, so duplicate entries add their product again, as in the
@@ -165,10 +167,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       __syncwarp();
     }
 
-    // ---- phase 1: dot products of the warp's rows with the window columns --
-    float2 dd[kRW][kPerLane];
+    // ---- phase 1: dot products of the block's rows with the window columns --
+    // Warps g and g + 4 take rows 8g .. 8g+7 (kRW2 rows a lane), the first and
+    // second half of each pass's columns of N: per 4 columns a lane loads 8 C
+    // slices (broadcasts) and 3 B slices for 24 products.
+    constexpr int kRW2 = 2 * kRW;
+    const int g8 = w & 3, half = w >> 2, r8 = g8 * kRW2;
+    float2 dd[kRW2][kPerLane];
 #pragma unroll
-    for (int r = 0; r < kRW; ++r)
+    for (int r = 0; r < kRW2; ++r)
 #pragma unroll
       for (int k = 0; k < kPerLane; ++k) dd[r][k] = make_float2(0.f, 0.f);
     for (int n0 = 0; n0 < N; n0 += kChunk) {
@@ -184,18 +191,19 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       cp_async_wait_all();
       __syncthreads();
-      if (r0 < nrows) {
+      if (r8 < nrows) {
         // rows past the block and window rows past the span read stale shared
         // memory; their sums are never used (masked or not stored)
-        for (int k4 = 0; k4 < q4; ++k4) {
-          float4 c[kRW], b[kPerLane];
+        const int kh = (q4 + 1) >> 1, k4a = half ? kh : 0, k4b = half ? q4 : kh;
+        for (int k4 = k4a; k4 < k4b; ++k4) {
+          float4 c[kRW2], b[kPerLane];
 #pragma unroll
-          for (int r = 0; r < kRW; ++r) c[r] = *reinterpret_cast<const float4*>(s_C + (r0 + r) * kStride + 4 * k4);
+          for (int r = 0; r < kRW2; ++r) c[r] = *reinterpret_cast<const float4*>(s_C + (r8 + r) * kStride + 4 * k4);
 #pragma unroll
           for (int k = 0; k < kPerLane; ++k)
             b[k] = *reinterpret_cast<const float4*>(s_win + (lane + 32 * k) * kStride + 4 * k4);
 #pragma unroll
-          for (int r = 0; r < kRW; ++r)
+          for (int r = 0; r < kRW2; ++r)
 #pragma unroll
             for (int k = 0; k < kPerLane; ++k) {
               dd[r][k] = __ffma2_rn(make_float2(c[r].x, c[r].y), make_float2(b[k].x, b[k].y), dd[r][k]);
@@ -204,22 +212,37 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
-    // the warp's tile: lane l owns window columns l, l + 32, l + 64
+    // the second half's sums reach the first half's warp through the window
+    // buffer (laid out [g][r][k][lane]); lane l owns window columns l, l + 32,
+    // l + 64; each value goes to the tile of the warp that owns its row
+    __syncthreads();  // every warp is done with the window rows
+    float* const xch = s_win;
+    if (half) {
 #pragma unroll
-    for (int k = 0; k < kPerLane; ++k) {
-      const int j = lane + 32 * k;
+      for (int r = 0; r < kRW2; ++r)
 #pragma unroll
-      for (int r = 0; r < kRW; ++r) {
-        const float v = dd[r][k].x + dd[r][k].y;
-        if constexpr (FUSED) {
-          const float cnt = aw[j * kRW + r];
-          aw[j * kRW + r] = cnt > 0.f ? cnt * v : 0.f;
-        } else {
-          aw[j * kRW + r] = v;
+        for (int k = 0; k < kPerLane; ++k) xch[((g8 * kRW2 + r) * kPerLane + k) * 32 + lane] = dd[r][k].x + dd[r][k].y;
+    }
+    __syncthreads();
+    if (!half) {
+#pragma unroll
+      for (int r = 0; r < kRW2; ++r) {
+        float* const ow = s_A + (2 * g8 + r / kRW) * (kSpan * kRW);  // the owning warp's tile
+        const int rr = r % kRW;
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) {
+          const int j = lane + 32 * k;
+          const float v = (dd[r][k].x + dd[r][k].y) + xch[((g8 * kRW2 + r) * kPerLane + k) * 32 + lane];
+          if constexpr (FUSED) {
+            const float cnt = ow[j * kRW + rr];
+            ow[j * kRW + rr] = cnt > 0.f ? cnt * v : 0.f;
+          } else {
+            ow[j * kRW + rr] = v;
+          }
         }
       }
     }
-    __syncwarp();
+    __syncthreads();  // every tile is complete
     if constexpr (!FUSED) {  // every stored (i, j) takes its dot product
       for (int r = r0; r < rend; ++r)
         for (int g = s_rp[r] + lane; g < s_rp[r + 1]; g += 32)
