@@ -229,6 +229,13 @@ spmm_status fusedmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const fl
     if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
     return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
   }
+  // Narrow rows: one thread per slice of each range, the dot products in the thread.
+  if (thread_ranges_shape(plan->N, false, vector_ok)) {
+    cudaError_t e = launch_thread_ranges_fused(L, vector_ok, Cd, B);
+    if (e == cudaSuccess && plan->split_event) e = cudaEventRecord(plan->split_event, stream);
+    if (e == cudaSuccess) e = launch_fixup(L);
+    return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+  }
   // Every column tile recomputes the dot products over all N columns, so wide
   // rows take one tile of up to 512 columns (two or four chunks per lane).
   Shape s = choose_shape_balanced(plan->N, false, vector_ok);

@@ -107,6 +107,8 @@ cudaError_t launch_rowgroup_f32(const Launch& L, int lanes);
 // fixup kernel completes rows split across ranges.
 bool thread_ranges_shape(int32_t N, bool bf16, bool vector_ok);
 cudaError_t launch_thread_ranges(const Launch& L, bool bf16, bool vector_ok);
+// FusedMM on the same shapes (fp32; L.B is D, Cd and Bd the dot-product operands).
+cudaError_t launch_thread_ranges_fused(const Launch& L, bool vector_ok, const float* Cd, const float* Bd);
 cudaError_t launch_rowgroup_bf16(const Launch& L, int lanes);
 cudaError_t launch_tc_window_bf16(const Launch& L);
 cudaError_t launch_window_f32(const Launch& L);

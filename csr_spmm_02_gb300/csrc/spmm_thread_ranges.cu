@@ -1,4 +1,4 @@
-// Instantiations of the thread-range SpMM kernel: the shapes where it beats the
+// Instantiations of the thread-range SpMM (and FusedMM) kernel: the shapes where it beats the
 // balanced kernel's lane groups (library A/B on the rmat20 and rmat22 patterns,
 // CUDA events, L2 flushed): N = 1 and 2 (scalar loads, fp32 or bf16 B) and N = 4
 // with 16-byte aligned fp32 B.  At N = 3, 5..8 the thread's row takes 4 or 8
@@ -16,6 +16,13 @@ cudaError_t launch_thread_ranges(const Launch& L, bool bf16, bool vector_ok) {
   if (L.N == 4) return launch_thread_ranges_t<float, 4, 1>(L);
   if (!bf16) return L.N == 1 ? launch_thread_ranges_t<float, 1, 1>(L) : launch_thread_ranges_t<float, 1, 2>(L);
   return L.N == 1 ? launch_thread_ranges_t<uint16_t, 1, 1>(L) : launch_thread_ranges_t<uint16_t, 1, 2>(L);
+}
+
+cudaError_t launch_thread_ranges_fused(const Launch& L, bool vector_ok, const float* Cd, const float* Bd) {
+  if (!thread_ranges_shape(L.N, false, vector_ok) || L.N < 1) return cudaErrorInvalidConfiguration;
+  if (L.N == 4) return launch_thread_ranges_t<float, 4, 1, true>(L, Cd, Bd);
+  return L.N == 1 ? launch_thread_ranges_t<float, 1, 1, true>(L, Cd, Bd)
+                  : launch_thread_ranges_t<float, 1, 2, true>(L, Cd, Bd);
 }
 
 }  // namespace spmm

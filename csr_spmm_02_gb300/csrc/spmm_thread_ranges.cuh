@@ -30,6 +30,12 @@
 //     inside the row).  The fixup kernel adds the slots of rows split across
 //     ranges, as for the balanced kernel.
 //
+// FusedMM mode (FusedMM section of the Intel Max page, Algorithm 3): the
+// value of nonzero (i, j) is the dot product C_i . B_j of two dense fp32
+// matrices, computed in the thread (a row of N <= 4 columns is local to it),
+// and the gathered rows belong to D; the walk, scan, slots and fixup are the
+// same.
+//
 // The summation order is fixed for a given plan (walk order in a thread, scan
 // tree across threads, range order in the fixup): C is bitwise reproducible.
 #pragma once
@@ -78,14 +84,21 @@ __host__ __device__ constexpr size_t thread_ranges_smem_bytes(int T, int VW) {
 
 // VEC columns per load (4: fp32 float4, 8: bf16 uint4, 1: scalar), NCH loads
 // per row, so a thread's row holds VW = VEC * NCH >= N columns.
-template <typename BT, int VEC, int NCH>
+template <typename BT, int VEC, int NCH, bool FUSED = false>
 __global__ void __launch_bounds__(kThreads)
     spmm_thread_ranges_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr,
                               const int32_t* __restrict__ colind, const float* __restrict__ vals,
                               const BT* __restrict__ B, float* __restrict__ C, const int2* __restrict__ part,
-                              int32_t T, float* __restrict__ carry, int* __restrict__ err) {
+                              int32_t T, float* __restrict__ carry, int* __restrict__ err,
+                              const float* __restrict__ Cd, const float* __restrict__ Bd) {
+  // FUSED: B is D (gathered and accumulated), Cd and Bd the dot-product
+  // operands, vals unused.
+  static_assert(!FUSED || sizeof(BT) == 4, "FusedMM is fp32");
   constexpr int VW = VEC * NCH;
-  constexpr int U = 8 / NCH > 0 ? 8 / NCH : 1;  // nonzeros whose B rows are in flight per thread
+  // nonzeros whose gathered rows are in flight per thread (FusedMM: three
+  // slices per nonzero, half as many)
+  constexpr int U0 = 8 / NCH > 0 ? 8 / NCH : 1;
+  constexpr int U = FUSED ? (U0 / 2 > 0 ? U0 / 2 : 1) : U0;
   constexpr int W = tr::kWarps;
 
   extern __shared__ __align__(16) unsigned char smem[];
@@ -119,10 +132,11 @@ __global__ void __launch_bounds__(kThreads)
   if (tid == 0) mbar_init(bar, 1);
   __syncthreads();
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar, (c_bulk ? 8u * uint32_t(cb - ca) : 0u) + (r_bulk ? 4u * uint32_t(rb - ra) : 0u));
+    mbar_arrive_expect_tx(bar, (c_bulk ? (FUSED ? 4u : 8u) * uint32_t(cb - ca) : 0u) +
+                                   (r_bulk ? 4u * uint32_t(rb - ra) : 0u));
     if (c_bulk) {
       bulk_g2s(smem_addr(s_col + (ca - nbase)), colind + ca, 4u * uint32_t(cb - ca), bar);
-      bulk_g2s(smem_addr(s_val + (ca - nbase)), vals + ca, 4u * uint32_t(cb - ca), bar);
+      if (!FUSED) bulk_g2s(smem_addr(s_val + (ca - nbase)), vals + ca, 4u * uint32_t(cb - ca), bar);
     }
     if (r_bulk) bulk_g2s(smem_addr(s_rp + (ra - rbase)), rowptr + ra, 4u * uint32_t(rb - ra), bar);
   }
@@ -130,12 +144,12 @@ __global__ void __launch_bounds__(kThreads)
     const int g = tid < 4 ? p0 + tid : cb + (tid - 4);
     if (tid < 8 && ((tid < 4 && g < ca) || (tid >= 4 && g < p1))) {
       s_col[g - nbase] = ld_stream(colind + g, stream_pol);
-      s_val[g - nbase] = ld_stream(vals + g, stream_pol);
+      if (!FUSED) s_val[g - nbase] = ld_stream(vals + g, stream_pol);
     }
   } else {
     for (int g = p0 + tid; g < p1; g += kThreads) {
       s_col[g - nbase] = ld_stream(colind + g, stream_pol);
-      s_val[g - nbase] = ld_stream(vals + g, stream_pol);
+      if (!FUSED) s_val[g - nbase] = ld_stream(vals + g, stream_pol);
     }
   }
   if (r_bulk) {
@@ -174,8 +188,12 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) coff[ch] = ch * VEC;
   const BT* brow0[NCH];
+  int cl[NCH];  // clamped column offsets (the dot-product operands' loads)
 #pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) brow0[ch] = B + min(coff[ch], N - VEC);
+  for (int ch = 0; ch < NCH; ++ch) {
+    cl[ch] = min(coff[ch], N - VEC);
+    brow0[ch] = B + cl[ch];
+  }
   float* const crow0 = C + size_t(i0) * N;
   auto store_row = [&](float* dst, const FVec<VEC> (&a)[NCH]) {
 #pragma unroll
@@ -207,21 +225,53 @@ __global__ void __launch_bounds__(kThreads)
     ++r;
     next_end = r < R ? rp[r + 1] : INT_MAX;
   };
+  int rc = r0, rc_end = rc < R ? rp[rc + 1] : INT_MAX;  // FusedMM: the row of the next nonzero to gather
   for (int j0 = n0; j0 < n1; j0 += U) {
     BSlice<BT, VEC> bs[U][NCH];
+    BSlice<float, VEC> bd[FUSED ? U : 1][NCH], cd[FUSED ? U : 1][NCH];
     float v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {  // gathers first (past n1: the batch's first nonzero again, unused)
-      const int k = (j0 + u < n1 ? j0 + u : j0) - nbase;
-      v[u] = s_val[k];
+      const int j = j0 + u < n1 ? j0 + u : j0;
+      const int k = j - nbase;
       const size_t roff = size_t(s_col[k]) * N;
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) bs[u][ch].load(brow0[ch] + roff);
+      if constexpr (FUSED) {
+        while (j >= rc_end) {  // rows are non-decreasing along the nonzeros
+          ++rc;
+          rc_end = rc < R ? rp[rc + 1] : INT_MAX;
+        }
+        const size_t coffr = size_t(i0 + rc) * N;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          bd[u][ch].load(Bd + roff + cl[ch]);
+          cd[u][ch].load(Cd + coffr + cl[ch]);
+        }
+      } else {
+        v[u] = s_val[k];
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (j0 + u >= n1) break;
       while (n == next_end) end_row();  // rows ending before this nonzero (empty rows too)
+      if constexpr (FUSED) {  // the value: C_row . B_col over the row's N columns
+        float d = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          FVec<VEC> x, y;
+          bd[u][ch].widen(x);
+          cd[u][ch].widen(y);
+          float t[VEC], q[VEC];
+          tr::to_floats<VEC>(x, t);
+          tr::to_floats<VEC>(y, q);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e)
+            if (coff[ch] + e < N) d = fmaf(q[e], t[e], d);
+        }
+        v[u] = d;
+      }
       FVec<VEC> b[NCH];
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) {
@@ -311,8 +361,8 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <typename BT, int VEC, int NCH>
-cudaError_t launch_thread_ranges_t(const Launch& L) {
+template <typename BT, int VEC, int NCH, bool FUSED = false>
+cudaError_t launch_thread_ranges_t(const Launch& L, const float* Cd = nullptr, const float* Bd = nullptr) {
   constexpr int VW = VEC * NCH;
   const size_t smem = thread_ranges_smem_bytes(L.items_per_cta, VW);
   static bool attr_set[kMaxDevices] = {};
@@ -320,16 +370,19 @@ cudaError_t launch_thread_ranges_t(const Launch& L) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= kMaxDevices || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(spmm_thread_ranges_kernel<BT, VEC, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(spmm_thread_ranges_kernel<BT, VEC, NCH, FUSED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(thread_ranges_smem_bytes(kMaxItemsPerCta, VW)));
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
-  SPMM_DEBUG_RANGES(L.stream, L.err, {{L.B, size_t(L.K) * L.N * sizeof(BT)}},
+  SPMM_DEBUG_RANGES(L.stream, L.err,
+                    {{L.B, size_t(L.K) * L.N * sizeof(BT)}, {Cd, FUSED ? size_t(L.M) * L.N * 4 : 0},
+                     {Bd, FUSED ? size_t(L.K) * L.N * 4 : 0}},
                     {{L.C, size_t(L.M) * L.N * 4}, {L.carry, size_t(L.num_ctas) * 2 * L.N * 4}});
-  spmm_thread_ranges_kernel<BT, VEC, NCH><<<unsigned(L.num_ctas), kThreads, smem, L.stream>>>(
+  spmm_thread_ranges_kernel<BT, VEC, NCH, FUSED><<<unsigned(L.num_ctas), kThreads, smem, L.stream>>>(
       L.M, L.N, L.rowptr, L.colind, L.vals, static_cast<const BT*>(L.B), L.C, L.part, L.items_per_cta, L.carry,
-      L.err);
+      L.err, Cd, Bd);
   return cudaGetLastError();
 }
 
