@@ -184,11 +184,11 @@ __global__ void __launch_bounds__(kThreads)
   locate(d0, r0, n0);
   locate(d1, r1, n1);
 
-  int coff[NCH];  // this thread's columns: VEC per load, clamped into the row for the loads
+  int coff[NCH];  // the row's columns, VEC per load (stores keep those below N)
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) coff[ch] = ch * VEC;
   const BT* brow0[NCH];
-  int cl[NCH];  // clamped column offsets (the dot-product operands' loads)
+  int cl[NCH];  // the same offsets clamped into the row, for every load
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
     cl[ch] = min(coff[ch], N - VEC);
