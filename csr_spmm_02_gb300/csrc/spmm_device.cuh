@@ -430,4 +430,69 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 
 
+// Stage one merge-path range of a CTA in shared memory: colind[p0, p1) at
+// s_col[g - (p0 & ~3)] and, with VALS, vals[p0, p1) at s_val[g - (p0 & ~3)];
+// rowptr[i0 .. i1] at s_rp[g - (i0 & ~3)].  The 16-byte aligned interiors go
+// by 1-D bulk copies (the TMA engine) that complete on the mbarrier s_bar,
+// initialised here for one arrival; the at most three unaligned entries at
+// each end, or everything when a pointer is misaligned, by plain loads (A is
+// read once: evict-first).  pre_barrier() runs before the first CTA barrier
+// (per-CTA shared state to set).  Returns false on every thread when the wait
+// for the copies gave up (kErrStageTimeout set in *err, after waiting again
+// for the copies in flight): the caller returns.  kThreads threads.
+template <bool VALS, typename Pre>
+__device__ __forceinline__ bool stage_range(const int32_t* __restrict__ colind, const float* __restrict__ vals,
+                                            const int32_t* __restrict__ rowptr, int i0, int p0, int i1, int p1,
+                                            int* s_col, float* s_val, int* s_rp, uint64_t* s_bar, int* err,
+                                            Pre pre_barrier) {
+  const int tid = threadIdx.x;
+  const int nbase = p0 & ~3, rbase = i0 & ~3;
+  const uint64_t stream_pol = policy_evict_first();
+  const uint32_t bar = smem_addr(s_bar);
+  const bool bulk_ok = ((reinterpret_cast<uintptr_t>(colind) | (VALS ? reinterpret_cast<uintptr_t>(vals) : 0) |
+                         reinterpret_cast<uintptr_t>(rowptr)) & 15) == 0;
+  const int ca = (p0 + 3) & ~3, cb = p1 & ~3;        // 16-byte aligned interior of [p0, p1)
+  const int ra = (i0 + 3) & ~3, rb = (i1 + 1) & ~3;  // ... of [i0, i1 + 1)
+  const bool c_bulk = bulk_ok && cb > ca;
+  const bool r_bulk = bulk_ok && rb > ra;
+  if (tid == 0) mbar_init(bar, 1);
+  pre_barrier();
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, (c_bulk ? (VALS ? 8u : 4u) * uint32_t(cb - ca) : 0u) +
+                                   (r_bulk ? 4u * uint32_t(rb - ra) : 0u));
+    if (c_bulk) {
+      bulk_g2s(smem_addr(s_col + (ca - nbase)), colind + ca, 4u * uint32_t(cb - ca), bar);
+      if (VALS) bulk_g2s(smem_addr(s_val + (ca - nbase)), vals + ca, 4u * uint32_t(cb - ca), bar);
+    }
+    if (r_bulk) bulk_g2s(smem_addr(s_rp + (ra - rbase)), rowptr + ra, 4u * uint32_t(rb - ra), bar);
+  }
+  if (c_bulk) {  // at most 3 leading and 3 trailing nonzeros
+    const int g = tid < 4 ? p0 + tid : cb + (tid - 4);
+    if (tid < 8 && ((tid < 4 && g < ca) || (tid >= 4 && g < p1))) {
+      s_col[g - nbase] = ld_stream(colind + g, stream_pol);
+      if (VALS) s_val[g - nbase] = ld_stream(vals + g, stream_pol);
+    }
+  } else {
+    for (int g = p0 + tid; g < p1; g += kThreads) {
+      s_col[g - nbase] = ld_stream(colind + g, stream_pol);
+      if (VALS) s_val[g - nbase] = ld_stream(vals + g, stream_pol);
+    }
+  }
+  if (r_bulk) {
+    const int g = tid < 4 ? i0 + tid : rb + (tid - 4);
+    if (tid < 8 && ((tid < 4 && g < ra) || (tid >= 4 && g <= i1))) s_rp[g - rbase] = ld_stream(rowptr + g, stream_pol);
+  } else {
+    for (int g = i0 + tid; g <= i1; g += kThreads) s_rp[g - rbase] = ld_stream(rowptr + g, stream_pol);
+  }
+  // (the test build's limit of one poll takes a single non-blocking look)
+  const bool staged = kStageSpinLimit <= 1 ? mbar_test(bar, 0) : mbar_wait_bounded(bar, 0, kStageSpinLimit);
+  if (__syncthreads_or(!staged)) {
+    if (tid == 0) atomicOr(err, kErrStageTimeout);
+    mbar_wait_bounded(bar, 0, kSpinLimit);  // let copies in flight land before leaving
+    return false;
+  }
+  return true;
+}
+
 }  // namespace spmm

@@ -231,37 +231,7 @@ __global__ void __launch_bounds__(kThreads, SPMM_SDDMM_MIN_BLOCKS)
   const uint64_t stream_pol = policy_evict_first();
 
   // ---- stage colind[p0, p1) and rowptr[i0, i1] ------------------------------
-  const uint32_t bar = smem_addr(s_bar);
-  const bool bulk_ok = ((reinterpret_cast<uintptr_t>(colind) | reinterpret_cast<uintptr_t>(rowptr)) & 15) == 0;
-  const int ca = (p0 + 3) & ~3, cb = p1 & ~3;
-  const int ra = (i0 + 3) & ~3, rb = (i1 + 1) & ~3;
-  const bool c_bulk = bulk_ok && cb > ca;
-  const bool r_bulk = bulk_ok && rb > ra;
-  if (tid == 0) mbar_init(bar, 1);
-  __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, (c_bulk ? 4u * uint32_t(cb - ca) : 0u) + (r_bulk ? 4u * uint32_t(rb - ra) : 0u));
-    if (c_bulk) bulk_g2s(smem_addr(s_col + (ca - nbase)), colind + ca, 4u * uint32_t(cb - ca), bar);
-    if (r_bulk) bulk_g2s(smem_addr(s_rp + (ra - rbase)), rowptr + ra, 4u * uint32_t(rb - ra), bar);
-  }
-  if (c_bulk) {
-    const int g = tid < 4 ? p0 + tid : cb + (tid - 4);
-    if (tid < 8 && ((tid < 4 && g < ca) || (tid >= 4 && g < p1))) s_col[g - nbase] = ld_stream(colind + g, stream_pol);
-  } else {
-    for (int g = p0 + tid; g < p1; g += kThreads) s_col[g - nbase] = ld_stream(colind + g, stream_pol);
-  }
-  if (r_bulk) {
-    const int g = tid < 4 ? i0 + tid : rb + (tid - 4);
-    if (tid < 8 && ((tid < 4 && g < ra) || (tid >= 4 && g <= i1))) s_rp[g - rbase] = ld_stream(rowptr + g, stream_pol);
-  } else {
-    for (int g = i0 + tid; g <= i1; g += kThreads) s_rp[g - rbase] = ld_stream(rowptr + g, stream_pol);
-  }
-  const bool staged = mbar_wait_bounded(bar, 0, kSpinLimit);
-  if (__syncthreads_or(!staged)) {
-    if (tid == 0) atomicOr(err, kErrStageTimeout);
-    mbar_wait_bounded(bar, 0, kSpinLimit);
-    return;
-  }
+  if (!stage_range<false>(colind, nullptr, rowptr, i0, p0, i1, p1, s_col, nullptr, s_rp, s_bar, err, [] {})) return;
   fill_row_ids(s_rp + (i0 - rbase), i1 - i0, p0, p1, nbase, s_row);
 
   // ---- rounds of nonzeros ---------------------------------------------------

@@ -121,49 +121,8 @@ __global__ void __launch_bounds__(kThreads)
   const int nbase = p0 & ~3, rbase = i0 & ~3;
   const uint64_t stream_pol = policy_evict_first();
 
-  // ---- 1. stage the range (as the balanced kernel) --------------------------
-  const uint32_t bar = smem_addr(s_bar);
-  const bool bulk_ok = ((reinterpret_cast<uintptr_t>(colind) | reinterpret_cast<uintptr_t>(vals) |
-                         reinterpret_cast<uintptr_t>(rowptr)) & 15) == 0;
-  const int ca = (p0 + 3) & ~3, cb = p1 & ~3;
-  const int ra = (i0 + 3) & ~3, rb = (i1 + 1) & ~3;
-  const bool c_bulk = bulk_ok && cb > ca;
-  const bool r_bulk = bulk_ok && rb > ra;
-  if (tid == 0) mbar_init(bar, 1);
-  __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, (c_bulk ? (FUSED ? 4u : 8u) * uint32_t(cb - ca) : 0u) +
-                                   (r_bulk ? 4u * uint32_t(rb - ra) : 0u));
-    if (c_bulk) {
-      bulk_g2s(smem_addr(s_col + (ca - nbase)), colind + ca, 4u * uint32_t(cb - ca), bar);
-      if (!FUSED) bulk_g2s(smem_addr(s_val + (ca - nbase)), vals + ca, 4u * uint32_t(cb - ca), bar);
-    }
-    if (r_bulk) bulk_g2s(smem_addr(s_rp + (ra - rbase)), rowptr + ra, 4u * uint32_t(rb - ra), bar);
-  }
-  if (c_bulk) {  // at most 3 leading and 3 trailing nonzeros
-    const int g = tid < 4 ? p0 + tid : cb + (tid - 4);
-    if (tid < 8 && ((tid < 4 && g < ca) || (tid >= 4 && g < p1))) {
-      s_col[g - nbase] = ld_stream(colind + g, stream_pol);
-      if (!FUSED) s_val[g - nbase] = ld_stream(vals + g, stream_pol);
-    }
-  } else {
-    for (int g = p0 + tid; g < p1; g += kThreads) {
-      s_col[g - nbase] = ld_stream(colind + g, stream_pol);
-      if (!FUSED) s_val[g - nbase] = ld_stream(vals + g, stream_pol);
-    }
-  }
-  if (r_bulk) {
-    const int g = tid < 4 ? i0 + tid : rb + (tid - 4);
-    if (tid < 8 && ((tid < 4 && g < ra) || (tid >= 4 && g <= i1))) s_rp[g - rbase] = ld_stream(rowptr + g, stream_pol);
-  } else {
-    for (int g = i0 + tid; g <= i1; g += kThreads) s_rp[g - rbase] = ld_stream(rowptr + g, stream_pol);
-  }
-  const bool staged = kStageSpinLimit <= 1 ? mbar_test(bar, 0) : mbar_wait_bounded(bar, 0, kStageSpinLimit);
-  if (__syncthreads_or(!staged)) {
-    if (tid == 0) atomicOr(err, kErrStageTimeout);
-    mbar_wait_bounded(bar, 0, kSpinLimit);  // let copies in flight land before leaving
-    return;
-  }
+  // ---- 1. stage the range ----------------------------------------------------
+  if (!stage_range<!FUSED>(colind, vals, rowptr, i0, p0, i1, p1, s_col, s_val, s_rp, s_bar, err, [] {})) return;
 
   // ---- 2. this thread's items -----------------------------------------------
   const int* rp = s_rp + (i0 - rbase);  // rp[r] = rowptr[i0 + r], 0 <= r <= R
