@@ -169,6 +169,13 @@ spmm_status sddmm(spmm_plan_t plan, int32_t K, const int32_t* colind, const floa
     while (nch < 4 && 32 * 4 * nch < plan->N) nch <<= 1;
     s = Shape{4, 32, nch};
   }
+  // Fewer lanes per dot product, each with more of the row: 8 lanes of N / 32
+  // chunks at N = 64 and 128 (4 nonzeros a warp step), 4 lanes of two chunks
+  // at N = 32; shorter reductions and more nonzeros per step (rmat20 at
+  // N = 128 1,018 -> 572 us, its pattern at N = 64 521 -> 358 us, rmat22 at
+  // N = 32 965 -> 924 us).
+  if (vector_ok && (plan->N == 32 || plan->N == 64 || plan->N == 128))
+    s = plan->N == 32 ? Shape{4, 4, 2} : Shape{4, 8, plan->N / 32};
   const cudaError_t e = launch_sddmm_f32(L, s, Cd, out);
   return e == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
 }

@@ -10,6 +10,7 @@ cudaError_t launch_sddmm_f32(const Launch& L, Shape s, const float* Cd, float* o
   SPMM_VECTOR_SHAPES(X, 4, SPMM_BAL_CHUNKS)
   SPMM_SCALAR_SHAPES(X)
   X(4, 32, 2) X(4, 32, 4)  // wide rows
+  X(4, 4, 2) X(4, 8, 2) X(4, 8, 4)  // two or four chunks per lane at N = 32, 64, 128
 #undef X
   return cudaErrorInvalidConfiguration;
 }
