@@ -38,7 +38,11 @@
 // FusedMM mode (same page, FusedMM section, Fig. 6, Algorithm 3, Fig. 11):
 // the sparse value of each nonzero (i, j) is not read from vals but computed
 // as the SDDMM dot product C_i . B_j of two dense fp32 matrices, and the
-// gathered rows belong to a third matrix D; the values are never stored.
+// gathered rows belong to a third matrix D.  After staging, the CTA computes
+// the values of all its nonzeros into the shared-memory slots that vals
+// would fill (the SDDMM kernel's rounds, spmm_sddmm.cuh, with the SDDMM
+// kernel's lane shape for the width), then streams the range exactly as for
+// SpMM; the values never leave the CTA.
 //
 // No floating-point atomics anywhere, so C is bitwise reproducible for a given
 // plan.
@@ -53,18 +57,13 @@
 #ifndef SPMM_BAL_LOADS
 #define SPMM_BAL_LOADS 8  // 16-byte B loads in flight per lane (U steps x NCH chunks)
 #endif
-#ifndef SPMM_FUSED_LOADS
-#define SPMM_FUSED_LOADS 4  // FusedMM: steps per batch (three 16-byte operand slices each)
-#endif
 #ifndef SPMM_BAL_MIN_BLOCKS
 #define SPMM_BAL_MIN_BLOCKS 4  // resident CTAs asked of the compiler (fp32, one chunk per lane)
 #endif
 #ifndef SPMM_BAL_ROW_WEIGHT
 #define SPMM_BAL_ROW_WEIGHT 0  // items a row end counts for in the warps' split (0: by shape, below)
 #endif
-#ifndef SPMM_FUSED_MIN_BLOCKS
-#define SPMM_FUSED_MIN_BLOCKS 3  // the same for FusedMM (80 registers)
-#endif
+
 
 namespace spmm {
 
@@ -72,23 +71,30 @@ namespace spmm {
 constexpr int kSlotHead = 1;    // the row began before the warp and ends in it
 constexpr int kSlotMiddle = 2;  // the warp lies entirely inside the row
 
-template <int NCH, bool FUSED = false>
+template <int NCH>
 struct BalancedSteps {
-  static constexpr int kLoads = FUSED ? SPMM_FUSED_LOADS : SPMM_BAL_LOADS;
-  static constexpr int value = kLoads / NCH > 0 ? kLoads / NCH : 1;
+  static constexpr int value = SPMM_BAL_LOADS / NCH > 0 ? SPMM_BAL_LOADS / NCH : 1;
+};
+
+// FusedMM's value pass: the lane shape the SDDMM kernel takes for the same
+// width (fewer lanes per dot product, each with more of the row).
+template <int VEC, int G, int NCH>
+struct FusedValueShape {
+  static constexpr bool narrow = VEC == 4 && NCH == 1 && (G == 8 || G == 16 || G == 32);
+  static constexpr int g = !narrow ? G : G == 8 ? 4 : 8;
+  static constexpr int nch = !narrow ? NCH : G == 8 ? 2 : G / 8;
 };
 
 // The 64-register budget of 4 resident CTAs fits the fp32 one-chunk SpMM
 // shapes without spills; wider or bf16 lanes keep the compiler's choice.
-// FusedMM (two gathered operands per nonzero plus the C slices) runs 3 CTAs
-// of 80 registers where its one-chunk, multi-lane shapes fit them (more
-// gathers in flight per SM than 2 CTAs of 128 registers, without the spills
-// of 4); the shapes that would spill more (one lane per nonzero, two or more
-// chunks per lane) keep 2.
+// FusedMM (value pass and walk in one kernel): 4 CTAs for 8-lane groups
+// (rmat22, N = 32: 1,974 -> 1,840 us against 3 CTAs), 3 of 80 registers for
+// the other one-chunk shapes (rmat20, N = 128: 1,424 -> 1,416 us; its pattern
+// at N = 64: 817 -> 790 us), no spills there.
 template <typename BT, int G, int NCH, bool FUSED>
 struct BalancedMinBlocks {
-  static constexpr int fused = (NCH == 1 && G >= 2) ? SPMM_FUSED_MIN_BLOCKS : 2;
-  static constexpr int value = FUSED ? fused : (sizeof(BT) == 4 && NCH == 1) ? SPMM_BAL_MIN_BLOCKS : 1;
+  static constexpr int fused = G == 8 ? 4 : 3;
+  static constexpr int value = (sizeof(BT) == 4 && NCH == 1) ? (FUSED ? fused : SPMM_BAL_MIN_BLOCKS) : 1;
 };
 
 __host__ __device__ constexpr size_t balanced_smem_layout_bytes(int W, int TW, int T) {
@@ -106,15 +112,14 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>
                          const int2* __restrict__ part, int32_t T, float* __restrict__ carry,
                          int* __restrict__ err, const float* __restrict__ Cd, const float* __restrict__ Bd) {
   // FUSED: B is D (gathered and accumulated), Cd and Bd the SDDMM operands, vals
-  // unused (its staging area holds the local row of every staged nonzero).
+  // unused (its staging area holds the local row ids, then the computed values).
   // SR: semiring code (spmm_device.cuh); 0 = ordinary SpMM.
   static_assert(!FUSED || sizeof(BT) == 4, "FusedMM is fp32");
   static_assert(SR == 0 || (!FUSED && sizeof(BT) == 4), "semirings: fp32 SpMM only");
-  using DotSlice = BSlice<float, FUSED ? VEC : 1>;  // fp32 slices of the dot-product operands
   constexpr int S = 32 / G;                // nonzeros per warp step
   constexpr int W = kThreads / 32;         // warps (workers) per CTA
   constexpr int TW = G * VEC * NCH;        // columns per tile
-  constexpr int U = BalancedSteps<NCH, FUSED>::value;  // steps per batch
+  constexpr int U = BalancedSteps<NCH>::value;  // steps per batch
 
   extern __shared__ __align__(16) unsigned char smem[];
   const int Tpad = T + 8;
@@ -138,34 +143,41 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>
   if (!stage_range<!FUSED>(colind, vals, rowptr, i0, p0, i1, p1, s_col, s_val, s_rp, s_bar, err,
                            [&] { for (int k = tid; k < W; k += kThreads) s_meta[k] = make_int2(-1, 0); }))
     return;
-  // SpMM: column indices become the offsets of their B rows in VEC-element
-  // units (c * N / VEC < 2^32, which the launch checks), so that a gather's
-  // address is one multiply-add on a 32-bit offset (rmat22 826 -> 818 us,
-  // rmat20 543 -> 525 us).  FusedMM keeps the column indices: its extra
-  // registers for the offsets spilled and cost more than they saved.
-  if constexpr (!FUSED) {
+  const int w = tid >> 5;
+  const int lane = tid & 31;
+  const int grp = lane / G;       // which nonzero of a step this lane's group takes
+  const int gl = lane & (G - 1);  // lane within its group
+  const int* rp = s_rp + (i0 - rbase);  // rp[r] = rowptr[i0 + r], 0 <= r <= i1 - i0
+  // FusedMM: the value of every staged nonzero.  The local row ids go into the
+  // value slots first; each warp's rounds read the ids of their nonzeros
+  // before storing the values over them.
+  if constexpr (FUSED) {
+    int* const s_row = reinterpret_cast<int*>(s_val);
+    fill_row_ids(rp, i1 - i0, p0, p1, nbase, s_row);
+    using VS = FusedValueShape<VEC, G, NCH>;
+    sddmm_rounds<VEC, VS::g, VS::nch>(N, s_col, s_row, nbase, p0, p1, Cd + size_t(i0) * N, Bd, w, lane,
+                                      [&](int n, float x) { s_val[n - nbase] = x; });
+    __syncthreads();
+  }
+  // Column indices become the offsets of their B (FusedMM: D) rows in
+  // VEC-element units (c * N / VEC < 2^32, which the launch checks), so that a
+  // gather's address is one multiply-add on a 32-bit offset (rmat22 826 -> 818
+  // us, rmat20 543 -> 525 us).
+  {
     const uint32_t nv = uint32_t(N / VEC);
     for (int k = p0 - nbase + tid; k < p1 - nbase; k += kThreads) s_col[k] = int(uint32_t(s_col[k]) * nv);
     __syncthreads();
   }
 
   // ---- 2. this warp's sub-range ---------------------------------------------
-  const int w = tid >> 5;
-  const int lane = tid & 31;
-  const int grp = lane / G;       // which nonzero of a step this lane's group takes
-  const int gl = lane & (G - 1);  // lane within its group
-  const int* rp = s_rp + (i0 - rbase);  // rp[r] = rowptr[i0 + r], 0 <= r <= i1 - i0
-  int* const s_row = reinterpret_cast<int*>(s_val);
-  if constexpr (FUSED) fill_row_ids(rp, i1 - i0, p0, p1, nbase, s_row);
   // The warps split the range's merged sequence with each row end counted as
   // kRowWeight items: row r's end sits at cost E(r) = (rowptr[r+1] - p0) +
   // kRowWeight * r, and a warp starting at cost c begins at the first row with
   // E(r) >= c and at the nonzeros of that row whose cost lies below c.  A row
   // end costs a warp about two steps (its butterfly and store) and a step
   // takes S nonzeros, so a row end weighs 2S nonzeros (capped at 16; measured
-  // best on rmat22 at S = 4 and rmat20 at S = 1).  FusedMM spends far more on
-  // each nonzero and keeps the plain merge path (weight 1).
-  constexpr int kRowWeight = SPMM_BAL_ROW_WEIGHT > 0 ? SPMM_BAL_ROW_WEIGHT : FUSED ? 1 : (2 * S < 16 ? 2 * S : 16);
+  // best on rmat22 at S = 4 and rmat20 at S = 1).
+  constexpr int kRowWeight = SPMM_BAL_ROW_WEIGHT > 0 ? SPMM_BAL_ROW_WEIGHT : (2 * S < 16 ? 2 * S : 16);
   const int cost = (p1 - p0) + kRowWeight * (i1 - i0);
   auto find_row = [&](int c) {  // first local row whose end costs c or more
     int lo = 0, hi = i1 - i0;
@@ -193,66 +205,6 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>
   }
   const int* colw = s_col - nbase + grp;  // colw[a] = colind of nonzero a + grp (staged)
   const float* valw = s_val - nbase + grp;
-  // FusedMM: this lane's columns of the dot-product operands (first tile).
-  int dcoff[NCH];
-  bool dvalid[NCH];
-#pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) {
-    const int col = (ch * G + gl) * VEC;
-    dvalid[ch] = col < N;
-    dcoff[ch] = min(col, N - VEC);
-  }
-  const float* const Crow0 = FUSED ? Cd + size_t(i0) * N : nullptr;
-  // Issue the loads of both dot-product operand slices of the nonzero staged at index k.
-  auto load_dot = [&](int k, DotSlice (&bd)[NCH], DotSlice (&cd)[NCH]) {
-    if constexpr (FUSED) {
-      const size_t boff = size_t(s_col[k]) * N;
-      const size_t coff = size_t(s_row[k]) * N;
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        bd[ch].load(Bd + boff + dcoff[ch]);
-        cd[ch].load(Crow0 + coff + dcoff[ch]);
-      }
-    }
-  };
-  // Values of the U steps starting at q: each lane's partial dot products,
-  // summed over its group by the transposed butterfly, then handed to the
-  // group's lanes one step at a time (all lanes take part).
-  auto fused_values = [&](int q, const DotSlice (&bd)[FUSED ? U : 1][NCH], const DotSlice (&cd)[FUSED ? U : 1][NCH],
-                          float (&v)[FUSED ? U : 1]) {
-    if constexpr (FUSED) {
-      constexpr int P = U < G ? U : G;  // values a lane ends with: steps gl % P of each round of P
-      float d[U];
-#pragma unroll
-      for (int s = 0; s < U; ++s) {
-        FVec<VEC> b[NCH], c[NCH];
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          bd[s][ch].widen(b[ch]);
-          cd[s][ch].widen(c[ch]);
-        }
-        d[s] = dot_lane<VEC, NCH>(c, b, dvalid);
-        if (N > G * VEC * NCH) {
-          const int k = min(q + s * S + grp, pw1 - 1) - nbase;
-          d[s] += dot_tail_tiles<VEC, G, NCH>(Crow0 + size_t(s_row[k]) * N, Bd + size_t(s_col[k]) * N, N, gl);
-        }
-      }
-      if constexpr (G == 1) {
-#pragma unroll
-        for (int s = 0; s < U; ++s) v[s] = d[s];
-      } else {
-#pragma unroll
-        for (int r0 = 0; r0 < U; r0 += P) {
-          float t[P];
-#pragma unroll
-          for (int i = 0; i < P; ++i) t[i] = d[r0 + i];
-          const float x = group_reduce_transposed<G, P>(t, gl);
-#pragma unroll
-          for (int i = 0; i < P; ++i) v[r0 + i] = __shfl_sync(0xffffffffu, x, grp * G + i);
-        }
-      }
-    }
-  };
   auto slot_ptr = [&](int worker, int ch) { return s_slot + worker * TW + (ch * G + gl) * VEC; };
   FVec<VEC> acc[NCH];
   auto reset = [&](FVec<VEC>& a) {
@@ -332,19 +284,13 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>
   int q = pw0;
   for (; q + U * S <= pw1; q += U * S) {  // full batches
     BSlice<BT, VEC> bs[U][NCH];
-    DotSlice bd[FUSED ? U : 1][NCH], cd[FUSED ? U : 1][NCH];
-    float fv[FUSED ? U : 1];
 #pragma unroll
     for (int s = 0; s < U; ++s) {  // gathers first
-      const size_t roff = FUSED ? size_t(colw[q + s * S]) * N : size_t(uint32_t(colw[q + s * S])) * VEC;
+      const size_t roff = size_t(uint32_t(colw[q + s * S])) * VEC;
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
-      if constexpr (FUSED) load_dot(q + s * S + grp - nbase, bd[s], cd[s]);
     }
-    fused_values(q, bd, cd, fv);
-    auto value = [&](int s) {
-      if constexpr (FUSED) return fv[s]; else return valw[q + s * S];
-    };
+    auto value = [&](int s) { return valw[q + s * S]; };
     if (next_end > q + U * S) {  // no row ends inside the batch
 #pragma unroll
       for (int s = 0; s < U; ++s) {
@@ -363,24 +309,19 @@ __global__ void __launch_bounds__(kThreads, BalancedMinBlocks<BT, G, NCH, FUSED>
   }
   if (q < pw1) {  // short last batch: slots past the sub-range re-read its last nonzero's row, value 0
     BSlice<BT, VEC> bs[U][NCH];
-    DotSlice bd[FUSED ? U : 1][NCH], cd[FUSED ? U : 1][NCH];
-    float fv[FUSED ? U : 1];
 #pragma unroll
     for (int s = 0; s < U; ++s) {
       const int c = colw[min(q + s * S, pw1 - 1 - grp)];
-      const size_t roff = FUSED ? size_t(c) * N : size_t(uint32_t(c)) * VEC;
+      const size_t roff = size_t(uint32_t(c)) * VEC;
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) bs[s][ch].load(bl[ch] + roff);
-      if constexpr (FUSED) load_dot(min(q + s * S + grp, pw1 - 1) - nbase, bd[s], cd[s]);
     }
-    fused_values(q, bd, cd, fv);
 #pragma unroll
     for (int s = 0; s < U; ++s) {
       const int a = q + s * S;
       if (a >= pw1) break;
       const bool ok = a + grp < pw1;
-      float v;
-      if constexpr (FUSED) v = ok ? fv[s] : 0.f; else v = ok ? valw[a] : 0.f;
+      const float v = ok ? valw[a] : 0.f;
       step(a, v, ok, bs[s]);
     }
   }
@@ -441,9 +382,9 @@ cudaError_t launch_balanced_t(const Launch& L, const float* Cd = nullptr, const 
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
-  // SpMM keeps B-row offsets in 32 bits (VEC-element units): column c's row
-  // starts c * N / VEC vectors into B.
-  if (!FUSED && int64_t(L.K) * (L.N / VEC) > int64_t(UINT32_MAX)) return cudaErrorNotSupported;
+  // B-row offsets are kept in 32 bits (VEC-element units): column c's row
+  // starts c * N / VEC vectors into B (D for FusedMM).
+  if (int64_t(L.K) * (L.N / VEC) > int64_t(UINT32_MAX)) return cudaErrorNotSupported;
   const dim3 grid(unsigned(L.num_ctas), unsigned((L.N + TW - 1) / TW));
   SPMM_DEBUG_RANGES(L.stream, L.err,
                     {{L.B, size_t(L.K) * L.N * sizeof(BT)}, {Cd, FUSED ? size_t(L.M) * L.N * 4 : 0},

@@ -203,11 +203,18 @@ __device__ __forceinline__ void sddmm_round_dots(int base, int p1, int nbase, co
   }
 }
 
-template <int VEC, int G, int NCH>
-__global__ void __launch_bounds__(kThreads, SPMM_SDDMM_MIN_BLOCKS)
-    spmm_sddmm_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr, const int32_t* __restrict__ colind,
-                      const float* __restrict__ Cd, const float* __restrict__ B, float* __restrict__ out,
-                      const int2* __restrict__ part, int32_t T, int* __restrict__ err) {
+// The dot products of the staged nonzeros [p0, p1): nonzero n (staged at
+// n - nbase with column s_col and local row s_row) gets C_row . B_col, handed to
+// store(n, value).  Warp w takes rounds of 32 consecutive nonzeros (R steps of
+// S = 32/G, every S-th to each lane group), loads both operand rows of U steps
+// at a time and sums each group's partial products by the transposed
+// butterfly, after which lane l of a group holds nonzero l's value.  All of a
+// round's s_col / s_row reads come before its first store, and a warp reads
+// only its own rounds' entries, so store may overwrite them.
+template <int VEC, int G, int NCH, typename Store>
+__device__ __forceinline__ void sddmm_rounds(int N, const int* s_col, const int* s_row, int nbase, int p0, int p1,
+                                             const float* __restrict__ Crow0, const float* __restrict__ B, int w,
+                                             int lane, Store store) {
   constexpr int S = 32 / G;                     // nonzeros per warp step
   constexpr int W = kThreads / 32;
   constexpr int kLoads = G >= 32 ? SPMM_SDDMM_LOADS_WIDE : SPMM_SDDMM_LOADS;
@@ -215,27 +222,7 @@ __global__ void __launch_bounds__(kThreads, SPMM_SDDMM_MIN_BLOCKS)
   constexpr int R = G > U ? G : U;              // steps per warp iteration
   constexpr int NPI = R * S;                    // nonzeros per warp iteration
   static_assert(R % U == 0 && R % G == 0, "powers of two");
-
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int Tpad = T + 8;
-  int* s_col = reinterpret_cast<int*>(smem);
-  int* s_row = s_col + Tpad;
-  int* s_rp = s_col + 2 * Tpad;
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_col + 3 * Tpad);
-
-  const int tid = threadIdx.x;
-  const int2 beg = __ldg(part + blockIdx.x);
-  const int2 fin = __ldg(part + blockIdx.x + 1);
-  const int i0 = beg.x, p0 = beg.y, i1 = fin.x, p1 = fin.y;
-  const int nbase = p0 & ~3, rbase = i0 & ~3;
-  const uint64_t stream_pol = policy_evict_first();
-
-  // ---- stage colind[p0, p1) and rowptr[i0, i1] ------------------------------
-  if (!stage_range<false>(colind, nullptr, rowptr, i0, p0, i1, p1, s_col, nullptr, s_rp, s_bar, err, [] {})) return;
-  fill_row_ids(s_rp + (i0 - rbase), i1 - i0, p0, p1, nbase, s_row);
-
-  // ---- rounds of nonzeros ---------------------------------------------------
-  const int w = tid >> 5, lane = tid & 31, grp = lane / G, gl = lane & (G - 1);
+  const int grp = lane / G, gl = lane & (G - 1);
   int coffl[NCH];
   bool valid[NCH];
 #pragma unroll
@@ -244,7 +231,6 @@ __global__ void __launch_bounds__(kThreads, SPMM_SDDMM_MIN_BLOCKS)
     valid[ch] = col < N;
     coffl[ch] = min(col, N - VEC);
   }
-  const float* Crow0 = Cd + size_t(i0) * N;
   for (int base = p0 + w * NPI; base < p1; base += W * NPI) {
     float dots[R];
     // Rows are non-decreasing along the nonzeros: first == last means one row
@@ -267,9 +253,36 @@ __global__ void __launch_bounds__(kThreads, SPMM_SDDMM_MIN_BLOCKS)
       for (int i = 0; i < G; ++i) v[i] = dots[r0 + i];
       const float x = group_reduce_transposed<G, G>(v, gl);
       const int n = base + (r0 + gl) * S + grp;  // the warp's 32 lanes cover 32 consecutive nonzeros
-      if (n < p1) st_stream1(out + n, x);
+      if (n < p1) store(n, x);
     }
   }
+}
+
+template <int VEC, int G, int NCH>
+__global__ void __launch_bounds__(kThreads, SPMM_SDDMM_MIN_BLOCKS)
+    spmm_sddmm_kernel(int32_t M, int32_t N, const int32_t* __restrict__ rowptr, const int32_t* __restrict__ colind,
+                      const float* __restrict__ Cd, const float* __restrict__ B, float* __restrict__ out,
+                      const int2* __restrict__ part, int32_t T, int* __restrict__ err) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int Tpad = T + 8;
+  int* s_col = reinterpret_cast<int*>(smem);
+  int* s_row = s_col + Tpad;
+  int* s_rp = s_col + 2 * Tpad;
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_col + 3 * Tpad);
+
+  const int tid = threadIdx.x;
+  const int2 beg = __ldg(part + blockIdx.x);
+  const int2 fin = __ldg(part + blockIdx.x + 1);
+  const int i0 = beg.x, p0 = beg.y, i1 = fin.x, p1 = fin.y;
+  const int nbase = p0 & ~3, rbase = i0 & ~3;
+
+  // ---- stage colind[p0, p1) and rowptr[i0, i1] ------------------------------
+  if (!stage_range<false>(colind, nullptr, rowptr, i0, p0, i1, p1, s_col, nullptr, s_rp, s_bar, err, [] {})) return;
+  fill_row_ids(s_rp + (i0 - rbase), i1 - i0, p0, p1, nbase, s_row);
+
+  // ---- rounds of nonzeros ---------------------------------------------------
+  sddmm_rounds<VEC, G, NCH>(N, s_col, s_row, nbase, p0, p1, Cd + size_t(i0) * N, B, tid >> 5, tid & 31,
+                            [&](int n, float x) { st_stream1(out + n, x); });
 }
 
 template <int VEC, int G, int NCH>
