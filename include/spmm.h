@@ -103,7 +103,10 @@ typedef enum {
 
 /* Kernel family a plan uses. */
 typedef enum {
-  SPMM_KERNEL_AUTO = 0,      /* chosen from the row-length statistics */
+  SPMM_KERNEL_AUTO = 0,      /* chosen from the row-length statistics (rowptr only): skewed
+                              * rows -> BALANCED; even rows -> SMALLN for N <= 8, WINDOW_TC
+                              * for N >= 128 (which assumes local columns: on scattered
+                              * columns force ROW, faster there), else ROW */
   SPMM_KERNEL_ROW = 1,       /* one (sub-)warp group per row: short, uniform rows */
   SPMM_KERNEL_BALANCED = 2,  /* merge-path nnz-balanced split + fixup: skewed rows */
   SPMM_KERNEL_WINDOW = 3,    /* short rows, B rows reused across rows: a CTA of 32 rows
