@@ -151,12 +151,14 @@ constexpr int kDefaultItemsPerCta = 2048;
 // 2.05 -> 1.96 ms).  N = 1 and 4 run the thread-range kernel, whose CTAs
 // amortise their staging, searches and scan over more items at 3840 (15 per
 // thread; the rmat20 pattern at N = 1 119 -> 113 us, N = 4 167 -> 138 us);
-// N = 3 (lane groups) also gained there (165 -> 150 us).  2048 elsewhere:
-// N = 2, whose threads gather in batches of four (136 -> 206 us at 3840),
-// and N = 5 .. 8, 64 and 128.
+// N = 3 (lane groups) also gained there (165 -> 150 us), and so did N = 8 in
+// both of its kernels (fp32 B, lane groups: 226 -> 195 us; bf16 B, thread
+// ranges: 236 -> 185 us; rmat22 866 -> 783 and 941 -> 728 us).  2048
+// elsewhere: N = 2, whose threads gather in batches of four (136 -> 206 us at
+// 3840), and N = 5 .. 7, 64 and 128.
 inline int default_items_per_cta(int32_t N) {
   if (N > 8 && N <= 32) return 3072;
-  if (N == 1 || N == 3 || N == 4) return 3840;
+  if (N == 1 || N == 3 || N == 4 || N == 8) return 3840;
   return kDefaultItemsPerCta;
 }
 

@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(kThreads)
   int rc = r0, rc_end = rc < R ? rp[rc + 1] : INT_MAX;  // FusedMM: the row of the next nonzero to gather
   for (int j0 = n0; j0 < n1; j0 += U) {
     BSlice<BT, VEC> bs[U][NCH];
-    BSlice<float, VEC> bd[FUSED ? U : 1][NCH], cd[FUSED ? U : 1][NCH];
+    using DotSlice = BSlice<float, FUSED ? VEC : 1>;  // FusedMM's dot-product operands (fp32)
+    DotSlice bd[FUSED ? U : 1][NCH], cd[FUSED ? U : 1][NCH];
     float v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {  // gathers first (past n1: the batch's first nonzero again, unused)

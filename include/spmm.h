@@ -179,7 +179,7 @@ SPMM_API spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz
 /*
  * As spmm_csr_plan, with the kernel family forced (spmm_kernel value) and
  * the merge-path range size set: items_per_cta = 0 picks the default (3072
- * items for 8 < N <= 32, 3840 for N = 1, 3 and 4, else 2048), otherwise it must be a positive multiple of
+ * items for 8 < N <= 32, 3840 for N = 1, 3, 4 and 8, else 2048), otherwise it must be a positive multiple of
  * 256, at most 8192.
  */
 SPMM_API spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,

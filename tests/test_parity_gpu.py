@@ -139,13 +139,13 @@ def test_items_per_cta(T):
     H.assert_exact(C, H.reference(q)[0], f"integer T={T}")
 
 
-@pytest.mark.parametrize("N", [1, 2, 3, 4, 12, 24, 32, 64])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 8, 12, 24, 32, 64])
 def test_default_items_per_cta(N):
-    """The plan's own range size: 3072 items for 8 < N <= 32, 3840 for N = 1, 3, 4, else 2048."""
+    """The plan's own range size: 3072 items for 8 < N <= 32, 3840 for N = 1, 3, 4, 8, else 2048."""
     p = mixed(57, M=6000, K=3000, N=N)
     C, plan = H.run(p, kernel="balanced")
     info = plan.info()
-    T = 3072 if 8 < N <= 32 else 3840 if N in (1, 3, 4) else 2048
+    T = 3072 if 8 < N <= 32 else 3840 if N in (1, 3, 4, 8) else 2048
     assert info["items_per_cta"] == T and info["num_ctas"] == -(-(p.M + p.nnz) // T)
     C_ref, S = H.reference(p)
     H.assert_within(C, C_ref, S, "f32", f"default T, N={N}")

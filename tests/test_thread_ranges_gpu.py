@@ -1,13 +1,14 @@
 """The thread-range kernel: balanced plans with N <= 2 (fp32 or bf16 B, scalar
-loads) and N = 4 (16-byte aligned fp32 B), one thread per slice of each
-merge-path range.
+loads), N = 4 (16-byte aligned fp32 B) and N = 8 (16-byte aligned bf16 B), one
+thread per slice of each merge-path range.
 
 Range sizes of 256, 2048 and 8192 items (1, 8 and 32 items per thread), rows
 that end inside a thread, rows that cross threads, warps and ranges (long
 rows over many CTAs), empty rows and duplicates.  Small integers make every
 partial sum exact in fp32, so the result must equal the oracle's bit for bit
 whatever the summation order.  The neighbouring widths (N = 3, misaligned
-N = 4, N = 8), which stay on the lane-group kernel, are checked beside them.
+N = 4 and bf16 N = 8, fp32 N = 8), which stay on the lane-group kernel, are
+checked beside them.
 """
 import numpy as np
 import pytest
@@ -39,7 +40,7 @@ def test_exact_integers(N, b_dtype, T):
     plan.destroy()
 
 
-@pytest.mark.parametrize("N,b_dtype", [(1, "f32"), (2, "bf16"), (4, "f32")])
+@pytest.mark.parametrize("N,b_dtype", [(1, "f32"), (2, "bf16"), (4, "f32"), (8, "bf16")])
 def test_random_values_within_bound(N, b_dtype):
     p = _problem(500 + N, N, b_dtype, integer=False)
     C, plan = H.run(p, kernel="balanced", items_per_cta=2048)
@@ -48,13 +49,13 @@ def test_random_values_within_bound(N, b_dtype):
     plan.destroy()
 
 
-@pytest.mark.parametrize("N", [2, 4])
-def test_misaligned_b(N):
-    p = _problem(700 + N, N, "f32", integer=True)
+@pytest.mark.parametrize("N,b_dtype", [(2, "f32"), (4, "f32"), (8, "bf16")])
+def test_misaligned_b(N, b_dtype):
+    p = _problem(700 + N, N, b_dtype, integer=True)
     a = H.device_arrays(p)
-    flat = torch.empty(p.K * N + 1, device="cuda")
+    flat = torch.empty(p.K * N + 1, dtype=a["B"].dtype, device="cuda")
     flat[1:] = a["B"].reshape(-1)
-    a["B"] = flat[1:]  # 4 bytes past a 16-byte boundary
+    a["B"] = flat[1:]  # one element past a 16-byte boundary
     C, plan = H.run(p, kernel="balanced", items_per_cta=512, arrays=a)
     C_ref, _ = H.reference(p)
     H.assert_exact(C, C_ref, f"misaligned B, N={N}")
@@ -97,9 +98,9 @@ def test_deterministic():
     plan.destroy()
 
 
-@pytest.mark.parametrize("N", [1, 3, 4])
+@pytest.mark.parametrize("N", [1, 3, 4, 8])
 def test_default_ranges_for_sddmm_and_fusedmm(N):
-    """Plans at N = 1, 3 and 4 take 3840-item ranges by default; the merge-path
+    """Plans at N = 1, 3, 4 and 8 take 3840-item ranges by default; the merge-path
     SDDMM and fused kernels run on the same ranges."""
     import oracle
     p = _problem(900 + N, N, "f32", integer=True)
