@@ -680,6 +680,8 @@ def main(argv=None):
     ap.add_argument("--op", choices=["spmm", "sddmm", "fusedmm"], default="spmm")
     ap.add_argument("--kernel", choices=["auto", "row", "balanced", "window", "smalln", "window_tc"], default="auto")
     ap.add_argument("--n", type=int, default=0, help="dense width: redraw B with this many columns")
+    ap.add_argument("--b-dtype", choices=["f32", "bf16"], default=None,
+                    help="SpMM: redraw B in this type (default: the workload's own)")
     ap.add_argument("--semiring", default="sum,mul", help="(+),(x): sum|min|max , mul|add (SpMM only)")
     ap.add_argument("--group-lanes", type=int, default=0, help="lanes per row of a smalln plan")
     ap.add_argument("--column-tile", type=int, default=0, help="N-slicing: cap the column tile (row/balanced)")
@@ -697,14 +699,18 @@ def main(argv=None):
     if args.impl == "reference" and rank != 0:
         return 0  # rank 0 alone times the CPU oracle
     p = gen.make_workload(args.workload)
-    if args.n:  # same pattern and values, B redrawn with another width
+    redraw_dtype = args.b_dtype is not None and args.b_dtype != p.b_dtype
+    if redraw_dtype and args.op != "spmm":
+        raise SystemExit("--b-dtype applies to SpMM only (SDDMM and FusedMM take fp32 operands)")
+    if args.n or redraw_dtype:  # same pattern and values, B redrawn with another width or type
         import dataclasses
         import numpy as np
-        B = gen.uniform_b(np.random.default_rng(1000 + p.seed), p.K, args.n, p.b_dtype)
-        p = dataclasses.replace(p, N=args.n, B=B, name=f"{p.name}_n{args.n}")
+        nn, bd = args.n or p.N, args.b_dtype or p.b_dtype
+        B = gen.uniform_b(np.random.default_rng(1000 + p.seed), p.K, nn, bd)
+        p = dataclasses.replace(p, N=nn, B=B, b_dtype=bd, name=f"{p.name}_n{nn}" + ("_bf16" if redraw_dtype and bd == "bf16" else ""))
     name = args.workload if args.op == "spmm" else f"{args.workload} pattern, {args.op}"
-    if args.n:
-        name += f", B redrawn with N={args.n}"
+    if args.n or redraw_dtype:
+        name += f", B redrawn with N={p.N}" + (f" in {p.b_dtype}" if redraw_dtype else "")
     if args.semiring != ("sum", "mul"):
         name += f", semiring ({args.semiring[0]}, {args.semiring[1]})"
     cfg = {"workload": name, "M": p.M, "K": p.K, "N": p.N, "nnz": p.nnz,
