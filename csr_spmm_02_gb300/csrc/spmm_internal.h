@@ -102,9 +102,9 @@ cudaError_t launch_row_bf16(const Launch& L, Shape s);
 cudaError_t launch_balanced_f32(const Launch& L, Shape s);
 cudaError_t launch_balanced_bf16(const Launch& L, Shape s);
 cudaError_t launch_rowgroup_f32(const Launch& L, int lanes);
-// Balanced plans with N <= 2, or N = 4 with aligned fp32 B (thread_ranges_shape):
-// one thread per slice of each merge-path range (spmm_thread_ranges.cuh); the
-// fixup kernel completes rows split across ranges.
+// Balanced plans with N <= 2, N = 4 with aligned fp32 B or N = 8 with aligned
+// bf16 B (thread_ranges_shape): one thread per slice of each merge-path range
+// (spmm_thread_ranges.cuh); the fixup kernel completes rows split across ranges.
 bool thread_ranges_shape(int32_t N, bool bf16, bool vector_ok);
 cudaError_t launch_thread_ranges(const Launch& L, bool bf16, bool vector_ok);
 // FusedMM on the same shapes (fp32; L.B is D, Cd and Bd the dot-product operands).

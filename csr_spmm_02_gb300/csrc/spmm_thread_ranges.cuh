@@ -1,5 +1,6 @@
 // SpMM for narrow B on merge-path ranges: one thread per slice of the range
-// (balanced plans with N <= 2, and N = 4 with 16-byte aligned fp32 B).
+// (balanced plans with N <= 2, N = 4 with 16-byte aligned fp32 B and N = 8
+// with 16-byte aligned bf16 B).
 //
 // With N <= 8 a whole output row fits one thread's registers, so the
 // merge-path split can go down to threads: each of the CTA's 256 threads
