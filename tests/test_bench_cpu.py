@@ -1,5 +1,6 @@
 """bench.py's host-side pieces on CPU: the compulsory bytes and flops of each
-operation, the reference arm for every operation and option, and the
+operation, the reference arm for every operation and option (B redrawn in
+bf16 among them), and the
 per-kernel source hashes that key the traffic records."""
 import json
 
@@ -42,7 +43,7 @@ def test_dense_operands_are_seeded_fp32():
 
 @pytest.mark.parametrize("argv", [
     ["--op", "sddmm"], ["--op", "fusedmm"], ["--semiring", "min,add"], ["--n", "4"],
-    ["--n", "4", "--semiring", "max,mul"],
+    ["--n", "4", "--semiring", "max,mul"], ["--n", "8", "--b-dtype", "bf16"], ["--b-dtype", "bf16"],
 ])
 def test_reference_arm_lines(argv, capsys):
     assert bench.main(["--impl", "reference", "--workload", "uniform1k", "--steps", "1", "--warmup", "0"] + argv) == 0
@@ -51,7 +52,19 @@ def test_reference_arm_lines(argv, capsys):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     if "--n" in argv:
-        assert line["config"]["N"] == 4
+        assert line["config"]["N"] == int(argv[argv.index("--n") + 1])
+    if "--b-dtype" in argv:  # B redrawn in bf16: the compulsory bytes count 2-byte B elements
+        cfg = line["config"]
+        assert cfg["b_dtype"] == "bf16" and "in bf16" in cfg["workload"]
+        p = gen.make_workload("uniform1k")
+        assert cfg["compulsory_bytes"] == 4 * (p.M + 1) + 8 * p.nnz + 2 * p.K * cfg["N"] + 4 * p.M * cfg["N"]
+
+
+def test_b_dtype_is_refused_for_sddmm_and_fusedmm():
+    for op in ("sddmm", "fusedmm"):
+        with pytest.raises(SystemExit):
+            bench.main(["--impl", "reference", "--workload", "uniform1k", "--op", op, "--b-dtype", "bf16",
+                        "--steps", "1", "--warmup", "0"])
 
 
 def test_traffic_records_match_their_kernels():
