@@ -1,7 +1,7 @@
 """bench.py's host-side pieces on CPU: the compulsory bytes and flops of each
 operation, the reference arm for every operation and option (B redrawn in
-bf16 among them), and the
-per-kernel source hashes that key the traffic records."""
+bf16 among them), and the per-kernel source hashes that key the traffic
+records."""
 import json
 
 import numpy as np
