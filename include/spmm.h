@@ -180,7 +180,9 @@ SPMM_API spmm_status spmm_csr_plan(const int32_t* rowptr, int32_t M, int64_t nnz
  * As spmm_csr_plan, with the kernel family forced (spmm_kernel value) and
  * the merge-path range size set: items_per_cta = 0 picks the default (3072
  * items for 8 < N <= 32, 3840 for N = 1, 3, 4 and 8, else 2048), otherwise it must be a positive multiple of
- * 256, at most 8192.
+ * 256, at most 8192.  The default serves SpMM and FusedMM; a plan used only
+ * for SDDMM at N = 8 runs faster on 2048-item ranges (R-MAT patterns: about
+ * 5% at scale 20, 20% at scale 22).
  */
 SPMM_API spmm_status spmm_csr_plan_ex(const int32_t* rowptr, int32_t M, int64_t nnz, int32_t N,
                              int32_t kernel, int32_t items_per_cta, void* stream,
